@@ -1,0 +1,149 @@
+// Step 4 - combine ([RT] intranode/internodeCombine; [AR] 4.2 combine
+// routing).  combined_x[s][t] = bf16_rne(sum over contributing ranks r, in
+// ascending order, of float(y[recv_base[r] + send_pos[s][t][r]])).
+//
+// Work unit = (token, column slice of 32 x 16 bytes).  A warp reads the
+// token's send_pos row (lane r = rank r), compacts the contributing rows in
+// ascending rank order into shared memory, then each lane loads its 16-byte
+// chunk from every contributing row (all loads in flight together),
+// accumulates in fp32 in that order, rounds to bf16 and stores 16 bytes.
+// Slices of one token go to neighbouring warps, so every load of a warp is a
+// contiguous 512-byte segment.  No atomics: the result is deterministic and
+// bit-identical to a sequential fp32 sum in the same order.
+#include <cuda_bf16.h>
+
+#include "ep_device.cuh"
+#include "ep_internal.h"
+
+namespace ep {
+namespace {
+
+constexpr int kCombineThreads = 256;
+constexpr int kCombineWarps = kCombineThreads / kWarp;
+constexpr int kCombineBlocksPerSm = 3;
+constexpr int kBatch = 8;  // contributing rows loaded together
+
+struct CombineArgs {
+    const uint8_t* y;
+    const float* y_w;
+    const int32_t* send_pos;
+    const int64_t* recv_base;
+    uint8_t* out;
+    float* out_w;
+    int32_t* status;
+    long long y_rows;
+    int R, K;
+    long long row_bytes;
+    int chunks;  // 16-byte chunks per row
+    int slices;  // ceil(chunks / 32)
+    long long num_units;
+};
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += __uint_as_float(w[i] << 16);
+        acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(kCombineThreads, kCombineBlocksPerSm)
+combine_kernel(CombineArgs p) {
+    __shared__ long long s_base[33];
+    __shared__ long long s_rows[kCombineWarps][32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid <= p.R) s_base[tid] = p.recv_base[tid];
+    __syncthreads();
+    long long* rows = s_rows[warp];
+    const long long warps_total = static_cast<long long>(gridDim.x) * kCombineWarps;
+
+    for (long long u = static_cast<long long>(blockIdx.x) * kCombineWarps + warp; u < p.num_units;
+         u += warps_total) {
+        const long long g = u / p.slices;
+        const int slice = static_cast<int>(u - g * p.slices);
+        const int32_t sp = lane < p.R ? __ldg(p.send_pos + g * p.R + lane) : -1;
+        long long row = -1;
+        if (sp >= 0) {
+            row = s_base[lane] + sp;
+            if (row >= p.y_rows) {
+                flag_error(p.status, EP_DEV_CAPACITY);
+                row = -1;
+            } else if (row >= s_base[lane + 1]) {
+                flag_error(p.status, EP_DEV_INCONSISTENT);
+                row = -1;
+            }
+        }
+        const unsigned valid = __ballot_sync(0xffffffffu, row >= 0);
+        const int n = __popc(valid);
+        if (row >= 0) rows[__popc(valid & lanemask_lt())] = row;
+        __syncwarp();
+
+        const int ch = slice * kWarp + lane;
+        if (ch < p.chunks) {
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            const long long col = static_cast<long long>(ch) * 16;
+            for (int j0 = 0; j0 < n; j0 += kBatch) {
+                uint4 v[kBatch];
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i)
+                    if (j0 + i < n) v[i] = ld_nc_v4(p.y + rows[j0 + i] * p.row_bytes + col);
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i)
+                    if (j0 + i < n) add_bf16x8(acc, v[i]);
+            }
+            st_v4(p.out + g * p.row_bytes + col, pack_bf16x8(acc));
+        }
+        if (slice == 0 && p.out_w != nullptr && lane < p.K) {
+            float w = 0.0f;
+            for (int j = 0; j < n; ++j) w += __ldg(p.y_w + rows[j] * p.K + lane);
+            p.out_w[g * p.K + lane] = w;
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Shape& sh, const uint16_t* y, const float* y_w, int64_t y_rows,
+                           const int32_t* send_pos, const int64_t* recv_base, uint16_t* combined_x,
+                           float* combined_w, int32_t* status, cudaStream_t stream) {
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (tokens == 0) return cudaSuccess;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    CombineArgs p;
+    p.y = reinterpret_cast<const uint8_t*>(y);
+    p.y_w = y_w;
+    p.send_pos = send_pos;
+    p.recv_base = recv_base;
+    p.out = reinterpret_cast<uint8_t*>(combined_x);
+    p.out_w = combined_w;
+    p.status = status;
+    p.y_rows = y_rows;
+    p.R = sh.R;
+    p.K = sh.K;
+    p.row_bytes = sh.row_bytes();
+    p.chunks = static_cast<int>(p.row_bytes / 16);
+    p.slices = (p.chunks + kWarp - 1) / kWarp;
+    p.num_units = tokens * p.slices;
+    const long long want = (p.num_units + kCombineWarps - 1) / kCombineWarps;
+    const long long cap = static_cast<long long>(sms) * kCombineBlocksPerSm;
+    const long long grid = want < cap ? want : cap;
+    combine_kernel<<<static_cast<unsigned>(grid), kCombineThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

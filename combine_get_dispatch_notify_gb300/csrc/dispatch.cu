@@ -1,0 +1,272 @@
+// Step 3 - dispatch ([RT] intranode/internodeDispatch receive side; [AR] 4.1
+// SrcInfo).  Token (s,t) goes to pool row recv_base[r] + send_pos[s][t][r]
+// of every rank r it is routed to.
+//
+// Persistent CTAs walk work units (token, row part) with a stride of the
+// grid.  Each CTA runs a shared-memory ring of `slots` buffers fed by the TMA
+// engine (bulk, non-tensor copies):
+//   warp 0 (producer): reads the unit's send_pos row (lane r = rank r),
+//        resolves the destination rows, waits for a free slot and issues one
+//        bulk global->shared copy of the row part, completing on the slot's
+//        "full" mbarrier;
+//   warp 1 (storer, one thread): waits "full", issues one bulk
+//        shared->global copy per destination, commits them as a bulk group,
+//        and frees the previous slot once its group has been read out;
+//   warps 2-3 (metadata): write recv_topk_idx / recv_topk_w / recv_src_info
+//        for the destination rows of each token with plain stores.
+// Each row is read from HBM once and written once per destination; no
+// atomics decide placement (send_pos is precomputed by notify).  Every wait
+// is bounded; a wait that runs out sets EP_DEV_TIMEOUT and the CTA drains its
+// in-flight copies before exiting.
+#include "ep_device.cuh"
+#include "ep_internal.h"
+
+namespace ep {
+namespace {
+
+constexpr int kDispatchThreads = 128;
+constexpr int kMaxSlots = 16;
+constexpr int kCtasPerSm = 2;
+constexpr int kSmemBudget = 100 * 1024;   // per CTA: two CTAs per SM
+constexpr int kMaxPartBytes = 32 * 1024;
+
+struct SlotDesc {
+    int n;               // destinations in rows[], -1 = end of stream
+    uint32_t bytes;      // bytes of this part
+    long long part_off;  // byte offset of the part inside the row
+    long long rows[32];  // pool row per destination (-1 = skip)
+};
+
+struct DispatchArgs {
+    const uint8_t* x;
+    const int64_t* topk_idx;
+    const float* topk_w;
+    const int32_t* send_pos;
+    const int64_t* recv_base;
+    long long capacity;
+    uint8_t* recv_x;
+    int64_t* recv_topk_idx;
+    float* recv_topk_w;
+    int32_t* recv_src_info;
+    int32_t* status;
+    int R, T, K, E_loc, parts, slots;
+    uint32_t part_bytes;
+    long long row_bytes;
+    long long num_units;
+    long long wait_limit_ns;
+};
+
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = p.slots;
+    uint8_t* data = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * p.part_bytes);
+    uint64_t* empty = full + S;
+    SlotDesc* desc = reinterpret_cast<SlotDesc*>(empty + S);
+    long long* base = reinterpret_cast<long long*>(desc + S);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid <= p.R) base[tid] = p.recv_base[tid];
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        int k = 0;  // phases armed so far (loads, then the end marker)
+        bool ok = true;
+        for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const long long g = u / p.parts;
+            const int part = static_cast<int>(u - g * p.parts);
+            const int32_t sp = lane < p.R ? __ldg(p.send_pos + g * p.R + lane) : -1;
+            const unsigned valid = __ballot_sync(0xffffffffu, sp >= 0);
+            if (valid == 0u) continue;
+            const int slot = k % S;
+            if (k >= S) {
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait(&empty[slot], ((k / S) - 1) & 1, globaltimer_ns() + p.wait_limit_ns);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (sp >= 0) {
+                long long row = base[lane] + sp;
+                if (row >= p.capacity) {
+                    flag_error(p.status, EP_DEV_CAPACITY);
+                    row = -1;
+                } else if (row >= base[lane + 1]) {
+                    flag_error(p.status, EP_DEV_INCONSISTENT);
+                    row = -1;
+                }
+                desc[slot].rows[__popc(valid & lanemask_lt())] = row;
+            }
+            const long long off = static_cast<long long>(part) * p.part_bytes;
+            const long long left = p.row_bytes - off;
+            const uint32_t bytes = left < p.part_bytes ? static_cast<uint32_t>(left) : p.part_bytes;
+            if (lane == 0) {
+                desc[slot].n = __popc(valid);
+                desc[slot].bytes = bytes;
+                desc[slot].part_off = off;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[slot], bytes);
+                bulk_g2s(data + static_cast<size_t>(slot) * p.part_bytes, p.x + g * p.row_bytes + off,
+                         bytes, &full[slot]);
+            }
+            ++k;
+        }
+        if (ok) {  // end-of-stream marker
+            const int slot = k % S;
+            bool got = true;
+            if (k >= S && lane == 0)
+                got = mbar_wait(&empty[slot], ((k / S) - 1) & 1, globaltimer_ns() + p.wait_limit_ns);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (got) {
+                if (lane == 0) {
+                    desc[slot].n = -1;
+                    mbar_arrive(&full[slot]);
+                }
+                ++k;
+            } else {
+                ok = false;
+            }
+        }
+        if (lane == 0) {
+            if (!ok) flag_error(p.status, EP_DEV_TIMEOUT);
+            // Drain: the newest phase armed on each slot has completed, so no
+            // bulk copy into shared memory outlives the CTA.
+            for (int x = 0; x < S; ++x) {
+                const int phases = k > x ? (k - x + S - 1) / S : 0;
+                if (phases > 0 &&
+                    !mbar_wait(&full[x], (phases - 1) & 1, globaltimer_ns() + p.wait_limit_ns))
+                    flag_error(p.status, EP_DEV_TIMEOUT);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- storer ----------------
+        if (lane == 0) {
+            for (int k = 0;; ++k) {
+                const int slot = k % S;
+                if (!mbar_wait(&full[slot], (k / S) & 1, globaltimer_ns() + p.wait_limit_ns)) {
+                    flag_error(p.status, EP_DEV_TIMEOUT);
+                    break;
+                }
+                const int n = desc[slot].n;
+                if (n < 0) break;
+                fence_proxy_async_smem();
+                const uint8_t* src = data + static_cast<size_t>(slot) * p.part_bytes;
+                const uint32_t bytes = desc[slot].bytes;
+                const long long off = desc[slot].part_off;
+                for (int j = 0; j < n; ++j) {
+                    const long long row = desc[slot].rows[j];
+                    if (row >= 0) bulk_s2g(p.recv_x + row * p.row_bytes + off, src, bytes);
+                }
+                bulk_commit();
+                if (k >= 1) {
+                    bulk_wait_read<1>();
+                    mbar_arrive(&empty[(k - 1) % S]);
+                }
+            }
+            bulk_wait_all();
+        }
+    } else {
+        // ---------------- metadata ----------------
+        const int mw = warp - 2;
+        int i = 0;
+        for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            if (u % p.parts != 0) continue;
+            if ((i++ & 1) != mw) continue;
+            const long long g = u / p.parts;
+            const int s = static_cast<int>(g / p.T), t = static_cast<int>(g - static_cast<long long>(s) * p.T);
+            const int32_t sp = lane < p.R ? __ldg(p.send_pos + g * p.R + lane) : -1;
+            long long e = -1;
+            float w = 0.0f;
+            int owner = -1;
+            if (lane < p.K) {
+                e = __ldg(p.topk_idx + g * p.K + lane);
+                w = __ldg(p.topk_w + g * p.K + lane);
+                owner = e >= 0 ? static_cast<int>(e / p.E_loc) : -1;
+            }
+            unsigned m = __ballot_sync(0xffffffffu, sp >= 0);
+            while (m) {
+                const int r = __ffs(m) - 1;
+                m &= m - 1;
+                const long long row = base[r] + __shfl_sync(0xffffffffu, sp, r);
+                if (row >= p.capacity || row >= base[r + 1]) continue;
+                if (lane < p.K) {
+                    const bool here = owner == r;
+                    p.recv_topk_idx[row * p.K + lane] = here ? e - static_cast<long long>(r) * p.E_loc : -1;
+                    p.recv_topk_w[row * p.K + lane] = here ? w : 0.0f;
+                }
+                if (lane == 0) *reinterpret_cast<int2*>(p.recv_src_info + row * 2) = make_int2(s, t);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
+                            const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
+                            int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                            float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                            cudaStream_t stream) {
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (tokens == 0) return cudaSuccess;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const long long grid_target = static_cast<long long>(sms) * kCtasPerSm;
+    const long long row_bytes = sh.row_bytes();
+
+    // Row parts: at most 32 KB, and split further (down to 2 KB) while there
+    // are fewer than 8 units per CTA.  Parts are multiples of 16 bytes.
+    long long part = row_bytes < kMaxPartBytes ? row_bytes : kMaxPartBytes;
+    auto units_for = [&](long long pb) { return tokens * ((row_bytes + pb - 1) / pb); };
+    while (part > 2048 && units_for(part) < 8 * grid_target) part = ((part / 2) + 15) / 16 * 16;
+    const int parts = static_cast<int>((row_bytes + part - 1) / part);
+    int slots = static_cast<int>(kSmemBudget / part);
+    slots = slots < 2 ? 2 : (slots > kMaxSlots ? kMaxSlots : slots);
+
+    DispatchArgs p;
+    p.x = reinterpret_cast<const uint8_t*>(x);
+    p.topk_idx = topk_idx;
+    p.topk_w = topk_w;
+    p.send_pos = send_pos;
+    p.recv_base = recv_base;
+    p.capacity = capacity_rows;
+    p.recv_x = reinterpret_cast<uint8_t*>(recv_x);
+    p.recv_topk_idx = recv_topk_idx;
+    p.recv_topk_w = recv_topk_w;
+    p.recv_src_info = recv_src_info;
+    p.status = status;
+    p.R = sh.R;
+    p.T = sh.T;
+    p.K = sh.K;
+    p.E_loc = sh.E_loc;
+    p.parts = parts;
+    p.slots = slots;
+    p.part_bytes = static_cast<uint32_t>(part);
+    p.row_bytes = row_bytes;
+    p.num_units = tokens * parts;
+    p.wait_limit_ns = kDefaultWaitLimitNs;
+
+    const size_t smem = static_cast<size_t>(slots) * part + 2 * slots * sizeof(uint64_t) +
+                        slots * sizeof(SlotDesc) + 33 * sizeof(long long);
+    cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const long long grid = p.num_units < grid_target ? p.num_units : grid_target;
+    dispatch_kernel<<<static_cast<unsigned>(grid), kDispatchThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

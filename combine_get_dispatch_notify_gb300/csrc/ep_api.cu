@@ -1,0 +1,245 @@
+// C ABI of libep_gb300.so (declared in include/ep.h): argument checks on the
+// host, then one launch per step on the caller's stream.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ep.h"
+#include "ep_device.cuh"
+#include "ep_internal.h"
+
+namespace ep {
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+namespace {
+
+bool make_shape(const ep_shape_t* s, Shape* out) {
+    if (s == nullptr) return false;
+    const long long R = s->num_ranks, T = s->num_tokens, K = s->num_topk, E = s->num_experts,
+                    H = s->hidden, C = s->num_channels, A = s->expert_alignment;
+    if (R < 1 || R > 32) return false;
+    if (R > kNodeSize && R % kNodeSize != 0) return false;
+    if (T < 0 || R * T >= (1LL << 30)) return false;
+    if (K < 1 || K > 32) return false;
+    if (E < R || E % R != 0 || E > 8192) return false;
+    if (H < 8 || H % 8 != 0 || H > (1 << 24)) return false;
+    if (C < 1 || C > 4096) return false;
+    if (A < 1) return false;
+    out->R = static_cast<int>(R);
+    out->T = static_cast<int>(T);
+    out->K = static_cast<int>(K);
+    out->E = static_cast<int>(E);
+    out->H = static_cast<int>(H);
+    out->C = static_cast<int>(C);
+    out->align = static_cast<int>(A);
+    out->N = R <= kNodeSize ? 1 : static_cast<int>(R / kNodeSize);
+    out->E_loc = static_cast<int>(E / R);
+    return true;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned8(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+bool aligned4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// An array of `n` elements: any pointer (even NULL) when empty, else non-NULL
+// and aligned to `align` bytes.
+bool array_ok(const void* p, long long n, unsigned align) {
+    if (n == 0) return true;
+    return p != nullptr && (reinterpret_cast<uintptr_t>(p) & (align - 1u)) == 0;
+}
+
+ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+ep_status_t notify_common(const ep_shape_t* shape, const uint8_t* is_token_in_rank,
+                          const int32_t* num_tokens_per_rank, const int32_t* num_tokens_per_rdma_rank,
+                          const int32_t* num_tokens_per_expert, int32_t* rank_prefix_matrix,
+                          int32_t* gbl_channel_prefix_matrix, int32_t* rdma_channel_prefix_matrix,
+                          int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+                          int32_t* recv_channel_offset, int32_t* num_recv_tokens,
+                          int32_t* num_rdma_recv_tokens, int32_t* num_recv_tokens_per_expert,
+                          int64_t* recv_base, int32_t* send_pos, void* workspace,
+                          size_t workspace_bytes, int32_t* status, int32_t* host_num_recv_tokens,
+                          int stall_block, long long wait_limit_ns, cudaStream_t stream) {
+    Shape sh;
+    if (!make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    const long long tok_rank = static_cast<long long>(sh.R) * sh.T * sh.R;
+    if (!array_ok(is_token_in_rank, tok_rank, 16) || !aligned4(num_tokens_per_rank) ||
+        !aligned4(num_tokens_per_rdma_rank) || !aligned4(num_tokens_per_expert) ||
+        !aligned4(rank_prefix_matrix) || !aligned4(gbl_channel_prefix_matrix) ||
+        !aligned4(rdma_channel_prefix_matrix) || !aligned4(recv_gbl_rank_prefix_sum) ||
+        !aligned4(recv_rdma_rank_prefix_sum) || !aligned4(recv_channel_offset) ||
+        !aligned4(num_recv_tokens) || !aligned4(num_rdma_recv_tokens) ||
+        !aligned4(num_recv_tokens_per_expert) || !aligned8(recv_base) ||
+        !array_ok(send_pos, tok_rank, 4) || !aligned16(workspace) || !aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    if (host_num_recv_tokens != nullptr && !aligned4(host_num_recv_tokens)) return EP_ERR_INVALID_ARG;
+    if (workspace_bytes < notify_workspace_bytes(sh)) return EP_ERR_INVALID_ARG;
+    NotifyArgs a;
+    a.is_token_in_rank = is_token_in_rank;
+    a.num_tokens_per_rank = num_tokens_per_rank;
+    a.num_tokens_per_rdma_rank = num_tokens_per_rdma_rank;
+    a.num_tokens_per_expert = num_tokens_per_expert;
+    a.rank_prefix_matrix = rank_prefix_matrix;
+    a.gbl_channel_prefix_matrix = gbl_channel_prefix_matrix;
+    a.rdma_channel_prefix_matrix = rdma_channel_prefix_matrix;
+    a.recv_gbl_rank_prefix_sum = recv_gbl_rank_prefix_sum;
+    a.recv_rdma_rank_prefix_sum = recv_rdma_rank_prefix_sum;
+    a.recv_channel_offset = recv_channel_offset;
+    a.num_recv_tokens = num_recv_tokens;
+    a.num_rdma_recv_tokens = num_rdma_recv_tokens;
+    a.num_recv_tokens_per_expert = num_recv_tokens_per_expert;
+    a.recv_base = recv_base;
+    a.send_pos = send_pos;
+    a.status = status;
+    a.host_num_recv_tokens = host_num_recv_tokens;
+    return from_cuda(launch_notify(sh, a, workspace, stall_block, wait_limit_ns, stream));
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" {
+
+const char* ep_status_string(ep_status_t status) {
+    switch (status) {
+        case EP_OK: return "ok";
+        case EP_ERR_INVALID_ARG: return "invalid argument";
+        case EP_ERR_CUDA: return "CUDA runtime error";
+        case EP_ERR_CAPACITY: return "receive capacity exceeded";
+        case EP_ERR_TIMEOUT: return "device wait timed out";
+        case EP_ERR_INCONSISTENT: return "count inputs disagree with is_token_in_rank";
+        case EP_ERR_INPUT: return "expert id outside [-1, num_experts)";
+    }
+    return "unknown status";
+}
+
+ep_status_t ep_check_shape(const ep_shape_t* shape) {
+    ep::Shape sh;
+    return ep::make_shape(shape, &sh) ? EP_OK : EP_ERR_INVALID_ARG;
+}
+
+int32_t ep_num_nodes(const ep_shape_t* shape) {
+    ep::Shape sh;
+    return ep::make_shape(shape, &sh) ? sh.N : -1;
+}
+
+size_t ep_notify_workspace_bytes(const ep_shape_t* shape) {
+    ep::Shape sh;
+    return ep::make_shape(shape, &sh) ? ep::notify_workspace_bytes(sh) : 0;
+}
+
+ep_status_t ep_get_dispatch_layout(const ep_shape_t* shape, const int64_t* topk_idx,
+                                   int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank,
+                                   int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                                   int32_t* status, cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (!ep::array_ok(topk_idx, tokens * sh.K, 16) || !ep::aligned4(num_tokens_per_rank) ||
+        !ep::aligned4(num_tokens_per_rdma_rank) || !ep::aligned4(num_tokens_per_expert) ||
+        !ep::array_ok(is_token_in_rank, tokens * sh.R, 16) || !ep::aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    return ep::from_cuda(ep::launch_layout(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                           num_tokens_per_expert, is_token_in_rank, status, stream));
+}
+
+ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_in_rank,
+                               const int32_t* num_tokens_per_rank,
+                               const int32_t* num_tokens_per_rdma_rank,
+                               const int32_t* num_tokens_per_expert, int32_t* rank_prefix_matrix,
+                               int32_t* gbl_channel_prefix_matrix,
+                               int32_t* rdma_channel_prefix_matrix,
+                               int32_t* recv_gbl_rank_prefix_sum,
+                               int32_t* recv_rdma_rank_prefix_sum, int32_t* recv_channel_offset,
+                               int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+                               int32_t* num_recv_tokens_per_expert, int64_t* recv_base,
+                               int32_t* send_pos, void* workspace, size_t workspace_bytes,
+                               int32_t* status, int32_t* host_num_recv_tokens,
+                               cudaStream_t stream) {
+    return ep::notify_common(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                             num_tokens_per_expert, rank_prefix_matrix, gbl_channel_prefix_matrix,
+                             rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
+                             recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
+                             num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos,
+                             workspace, workspace_bytes, status, host_num_recv_tokens, -1,
+                             ep::kDefaultWaitLimitNs, stream);
+}
+
+ep_status_t ep_debug_notify_dispatch_stall(
+    const ep_shape_t* shape, const uint8_t* is_token_in_rank, const int32_t* num_tokens_per_rank,
+    const int32_t* num_tokens_per_rdma_rank, const int32_t* num_tokens_per_expert,
+    int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+    int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum,
+    int32_t* recv_rdma_rank_prefix_sum, int32_t* recv_channel_offset, int32_t* num_recv_tokens,
+    int32_t* num_rdma_recv_tokens, int32_t* num_recv_tokens_per_expert, int64_t* recv_base,
+    int32_t* send_pos, void* workspace, size_t workspace_bytes, int32_t* status,
+    int32_t stall_block, int32_t wait_limit_us, cudaStream_t stream) {
+    if (wait_limit_us < 1 || wait_limit_us > 2000000) return EP_ERR_INVALID_ARG;
+    return ep::notify_common(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                             num_tokens_per_expert, rank_prefix_matrix, gbl_channel_prefix_matrix,
+                             rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
+                             recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
+                             num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos,
+                             workspace, workspace_bytes, status, nullptr, stall_block,
+                             static_cast<long long>(wait_limit_us) * 1000LL, stream);
+}
+
+ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
+                        const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
+                        int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                        float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                        cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    if (capacity_rows < 0) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    const long long cap = capacity_rows;
+    if (!ep::array_ok(x, tokens * sh.H, 16) || !ep::array_ok(topk_idx, tokens * sh.K, 8) ||
+        !ep::array_ok(topk_w, tokens * sh.K, 4) || !ep::array_ok(send_pos, tokens * sh.R, 4) ||
+        !ep::aligned8(recv_base) || !ep::array_ok(recv_x, cap * sh.H, 16) ||
+        !ep::array_ok(recv_topk_idx, cap * sh.K, 8) || !ep::array_ok(recv_topk_w, cap * sh.K, 4) ||
+        !ep::array_ok(recv_src_info, cap * 2, 8) || !ep::aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    return ep::from_cuda(ep::launch_dispatch(sh, x, topk_idx, topk_w, send_pos, recv_base,
+                                             capacity_rows, recv_x, recv_topk_idx, recv_topk_w,
+                                             recv_src_info, status, stream));
+}
+
+ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* y_w,
+                       int64_t y_rows, const int32_t* send_pos, const int64_t* recv_base,
+                       uint16_t* combined_x, float* combined_w, int32_t* status,
+                       cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    if (y_rows < 0) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    // y (and y_w when combined_w is requested) hold y_rows rows; the kernel
+    // never reads a row at or beyond y_rows.
+    if (!ep::array_ok(y, y_rows * sh.H, 16) || !ep::array_ok(send_pos, tokens * sh.R, 4) ||
+        !ep::aligned8(recv_base) || !ep::array_ok(combined_x, tokens * sh.H, 16) ||
+        !ep::aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    if (combined_w != nullptr && !ep::array_ok(y_w, y_rows * sh.K, 4)) return EP_ERR_INVALID_ARG;
+    if (!ep::array_ok(combined_w, combined_w ? tokens * sh.K : 0, 4)) return EP_ERR_INVALID_ARG;
+    return ep::from_cuda(ep::launch_combine(sh, y, y_w, y_rows, send_pos, recv_base, combined_x,
+                                            combined_w, status, stream));
+}
+
+ep_status_t ep_sync_status(const int32_t* status, cudaStream_t stream) {
+    if (!ep::aligned4(status)) return EP_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return EP_ERR_CUDA;
+    int32_t h = 0;
+    if (cudaMemcpy(&h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return EP_ERR_CUDA;
+    if (h & EP_DEV_TIMEOUT) return EP_ERR_TIMEOUT;
+    if (h & EP_DEV_CAPACITY) return EP_ERR_CAPACITY;
+    if (h & EP_DEV_INPUT) return EP_ERR_INPUT;
+    if (h & EP_DEV_INCONSISTENT) return EP_ERR_INCONSISTENT;
+    return EP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Host-side interface between the C ABI (ep_api.cu) and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ep {
+
+struct Shape {
+    int R, T, K, E, H, C, align;
+    int N;      // nodes: max(1, R / 8)
+    int E_loc;  // experts per rank
+    long long row_bytes() const { return 2LL * H; }
+};
+
+// SM count of the current device (0 on error).
+int device_sm_count();
+
+cudaError_t launch_layout(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+                          int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                          uint8_t* is_token_in_rank, int32_t* status, cudaStream_t stream);
+
+struct NotifyArgs {
+    const uint8_t* is_token_in_rank;
+    const int32_t* num_tokens_per_rank;
+    const int32_t* num_tokens_per_rdma_rank;
+    const int32_t* num_tokens_per_expert;
+    int32_t* rank_prefix_matrix;
+    int32_t* gbl_channel_prefix_matrix;
+    int32_t* rdma_channel_prefix_matrix;
+    int32_t* recv_gbl_rank_prefix_sum;
+    int32_t* recv_rdma_rank_prefix_sum;
+    int32_t* recv_channel_offset;
+    int32_t* num_recv_tokens;
+    int32_t* num_rdma_recv_tokens;
+    int32_t* num_recv_tokens_per_expert;
+    int64_t* recv_base;
+    int32_t* send_pos;
+    int32_t* status;
+    int32_t* host_num_recv_tokens;
+};
+
+size_t notify_workspace_bytes(const Shape& sh);
+
+// `workspace` must hold notify_workspace_bytes(sh) bytes; the launcher clears
+// it on `stream` first.  stall_block < 0 for normal runs.
+cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace, int stall_block,
+                          long long wait_limit_ns, cudaStream_t stream);
+
+cudaError_t launch_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
+                            const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
+                            int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                            float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                            cudaStream_t stream);
+
+cudaError_t launch_combine(const Shape& sh, const uint16_t* y, const float* y_w, int64_t y_rows,
+                           const int32_t* send_pos, const int64_t* recv_base, uint16_t* combined_x,
+                           float* combined_w, int32_t* status, cudaStream_t stream);
+
+}  // namespace ep

@@ -1,0 +1,173 @@
+// Step 1 - layout counting ([RT] getDispatchLayout; count vectors of [IN]
+// notify_dispatch sm0 stage 3).
+//
+// One thread-block cluster per source rank s.  The cluster's CTAs split s's
+// tokens; each thread takes one token, reads its K expert ids, builds the
+// R-bit destination mask, writes the is_token_in_rank row, and adds to
+// shared-memory histograms (experts by smem atomics, ranks and nodes by warp
+// ballot + popc).  CTA 0 of the cluster then sums the CTAs' histograms
+// through distributed shared memory and writes the counts - no global
+// atomics and no pre-zeroed outputs.
+#include <cooperative_groups.h>
+
+#include "ep_device.cuh"
+#include "ep_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace ep {
+namespace {
+
+constexpr int kLayoutThreads = 256;
+constexpr int kMaxClusterCtas = 8;       // portable cluster size
+constexpr int kTokensPerCtaTarget = 1024;
+
+// 4 mask bits -> 4 bytes holding 0 or 1 (bit i -> byte i, little-endian).
+__device__ __forceinline__ uint32_t bits4_to_bytes(uint32_t b) {
+    return (b & 1u) | ((b & 2u) << 7) | ((b & 4u) << 14) | ((b & 8u) << 21);
+}
+
+__device__ __forceinline__ void write_membership_row(uint8_t* row, uint32_t mask, int R) {
+    if ((R & 15) == 0) {
+        for (int w = 0; w < R / 16; ++w) {
+            const uint32_t m = mask >> (16 * w);
+            uint4 v;
+            v.x = bits4_to_bytes(m & 0xfu);
+            v.y = bits4_to_bytes((m >> 4) & 0xfu);
+            v.z = bits4_to_bytes((m >> 8) & 0xfu);
+            v.w = bits4_to_bytes((m >> 12) & 0xfu);
+            *reinterpret_cast<uint4*>(row + 16 * w) = v;
+        }
+    } else if ((R & 3) == 0) {
+        for (int w = 0; w < R / 4; ++w)
+            *reinterpret_cast<uint32_t*>(row + 4 * w) = bits4_to_bytes((mask >> (4 * w)) & 0xfu);
+    } else {
+        for (int r = 0; r < R; ++r) row[r] = static_cast<uint8_t>((mask >> r) & 1u);
+    }
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, int N, int E_loc,
+              int tokens_per_cta, int32_t* __restrict__ num_tokens_per_rank,
+              int32_t* __restrict__ num_tokens_per_rdma_rank,
+              int32_t* __restrict__ num_tokens_per_expert, uint8_t* __restrict__ is_token_in_rank,
+              int32_t* status) {
+    extern __shared__ int32_t hist[];  // [E] experts | [R] ranks | [N] nodes
+    cg::cluster_group cluster = cg::this_cluster();
+    const int part = static_cast<int>(cluster.block_rank());
+    const int parts = static_cast<int>(cluster.num_blocks());
+    const int s = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int bins = E + R + N;
+    int32_t* h_expert = hist;
+    int32_t* h_rank = hist + E;
+    int32_t* h_node = h_rank + R;
+    for (int i = tid; i < bins; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+
+    const int t_begin = min(T, part * tokens_per_cta);
+    const int t_end = min(T, t_begin + tokens_per_cta);
+    int rank_acc = 0, node_acc = 0;  // lane r (lane n) accumulates rank r (node n)
+    bool bad = false;
+    for (int base = t_begin; base < t_end; base += blockDim.x) {
+        const int t = base + tid;
+        uint32_t mask = 0;
+        if (t < t_end) {
+            const int64_t* ids = topk_idx + (static_cast<int64_t>(s) * T + t) * K;
+            int k = 0;
+            if ((K & 1) == 0) {
+                for (; k < K; k += 2) {
+                    const longlong2 e2 = __ldg(reinterpret_cast<const longlong2*>(ids + k));
+                    const long long e[2] = {e2.x, e2.y};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (e[h] >= 0 && e[h] < E) {
+                            mask |= 1u << static_cast<int>(e[h] / E_loc);
+                            atomicAdd(&h_expert[e[h]], 1);
+                        } else if (e[h] != -1) {
+                            bad = true;
+                        }
+                    }
+                }
+            } else {
+                for (; k < K; ++k) {
+                    const long long e = __ldg(ids + k);
+                    if (e >= 0 && e < E) {
+                        mask |= 1u << static_cast<int>(e / E_loc);
+                        atomicAdd(&h_expert[e], 1);
+                    } else if (e != -1) {
+                        bad = true;
+                    }
+                }
+            }
+            write_membership_row(is_token_in_rank + (static_cast<int64_t>(s) * T + t) * R, mask, R);
+        }
+        uint32_t node_mask;
+        if (R <= kNodeSize) {
+            node_mask = mask != 0u ? 1u : 0u;
+        } else {
+            node_mask = 0;
+            for (int n = 0; n < N; ++n) node_mask |= ((mask >> (kNodeSize * n)) & 0xffu) ? (1u << n) : 0u;
+        }
+        for (int r = 0; r < R; ++r) {
+            const unsigned b = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
+            if (lane == r) rank_acc += __popc(b);
+        }
+        for (int n = 0; n < N; ++n) {
+            const unsigned b = __ballot_sync(0xffffffffu, (node_mask >> n) & 1u);
+            if (lane == n) node_acc += __popc(b);
+        }
+    }
+    if (lane < R && rank_acc) atomicAdd(&h_rank[lane], rank_acc);
+    if (lane < N && node_acc) atomicAdd(&h_node[lane], node_acc);
+    if (bad) flag_error(status, EP_DEV_INPUT);
+
+    cluster.sync();  // every CTA's partial histogram is complete and visible
+    if (part == 0) {
+        for (int i = tid; i < bins; i += blockDim.x) {
+            int32_t sum = 0;
+            for (int j = 0; j < parts; ++j) sum += cluster.map_shared_rank(hist, j)[i];
+            if (i < E)
+                num_tokens_per_expert[static_cast<int64_t>(s) * E + i] = sum;
+            else if (i < E + R)
+                num_tokens_per_rank[static_cast<int64_t>(s) * R + (i - E)] = sum;
+            else
+                num_tokens_per_rdma_rank[static_cast<int64_t>(s) * N + (i - E - R)] = sum;
+        }
+    }
+    cluster.sync();  // keep every histogram alive until CTA 0 has read it
+}
+
+}  // namespace
+
+cudaError_t launch_layout(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+                          int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                          uint8_t* is_token_in_rank, int32_t* status, cudaStream_t stream) {
+    int parts = (sh.T + kTokensPerCtaTarget - 1) / kTokensPerCtaTarget;
+    parts = parts < 1 ? 1 : (parts > kMaxClusterCtas ? kMaxClusterCtas : parts);
+    const int tokens_per_cta = (sh.T + parts - 1) / parts;
+    const size_t smem = sizeof(int32_t) * static_cast<size_t>(sh.E + sh.R + sh.N);
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(parts, sh.R, 1);
+    cfg.blockDim = dim3(kLayoutThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = parts;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, layout_kernel, topk_idx, sh.R, sh.T, sh.K, sh.E, sh.N, sh.E_loc,
+                              tokens_per_cta, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                              num_tokens_per_expert, is_token_in_rank, status);
+}
+
+}  // namespace ep

@@ -1,0 +1,335 @@
+"""Thin Python binding of libep_gb300.so (the C ABI in include/ep.h).
+
+Functions carry the C names and only marshal arguments: they check that each
+tensor is a contiguous CUDA tensor of the right dtype and shape, pass its
+device address and the current CUDA stream, and raise :class:`EpError` on a
+non-OK status.  Every step runs in the library's sm_103a kernels; there is no
+CPU path.  ``alloc_*`` helpers allocate output tensors with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libep_gb300.so")
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = -1
+EP_ERR_CUDA = -2
+EP_ERR_CAPACITY = -3
+EP_ERR_TIMEOUT = -4
+EP_ERR_INCONSISTENT = -5
+EP_ERR_INPUT = -6
+
+EP_DEV_CAPACITY = 0x1
+EP_DEV_TIMEOUT = 0x2
+EP_DEV_INCONSISTENT = 0x4
+EP_DEV_INPUT = 0x8
+
+NODE_SIZE = 8
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+
+
+class EpShape(ctypes.Structure):
+    """Mirror of ep_shape_t."""
+
+    _fields_ = [("num_ranks", _i32), ("num_tokens", _i32), ("num_topk", _i32),
+                ("num_experts", _i32), ("hidden", _i32), ("num_channels", _i32),
+                ("expert_alignment", _i32)]
+
+    @classmethod
+    def make(cls, R, T, K, E, H, C, expert_alignment=1) -> "EpShape":
+        return cls(R, T, K, E, H, C, expert_alignment)
+
+    @property
+    def N(self) -> int:
+        return 1 if self.num_ranks <= NODE_SIZE else self.num_ranks // NODE_SIZE
+
+    @property
+    def E_loc(self) -> int:
+        return self.num_experts // self.num_ranks
+
+
+class EpError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {ep_status_string(status)} ({status})")
+
+
+_SIGS = {
+    "ep_status_string": (ctypes.c_char_p, [_i32]),
+    "ep_check_shape": (_i32, [ctypes.POINTER(EpShape)]),
+    "ep_num_nodes": (_i32, [ctypes.POINTER(EpShape)]),
+    "ep_notify_workspace_bytes": (_sz, [ctypes.POINTER(EpShape)]),
+    "ep_get_dispatch_layout": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 6 + [_vp]),
+    "ep_notify_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_sz, _vp, _vp, _vp]),
+    "ep_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 5 + [_vp]),
+    "ep_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i64] + [_vp] * 5 + [_vp]),
+    "ep_sync_status": (_i32, [_vp, _vp]),
+    "ep_debug_notify_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 +
+                                       [_sz, _vp, _i32, _i32, _vp]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libep_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c \"import "
+                               "__graft_entry__ as g; g.build()\"` (needs nvcc)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def exported_symbols() -> list[str]:
+    return list(_SIGS)
+
+
+# --------------------------------------------------------------------------- helpers
+def _stream(stream) -> _vp:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _vp(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _t(t: torch.Tensor | None, dtype, shape, name: str, nullable=False) -> _vp:
+    if t is None:
+        if nullable:
+            return _vp(None)
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return _vp(t.data_ptr())
+
+
+def _rows(t: torch.Tensor, name: str) -> int:
+    if t.dim() < 1:
+        raise ValueError(f"{name} must have a row axis")
+    return t.shape[0]
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != EP_OK:
+        raise EpError(fn, rc)
+
+
+# --------------------------------------------------------------------------- C names
+def ep_status_string(status: int) -> str:
+    return lib().ep_status_string(status).decode()
+
+
+def ep_check_shape(shape: EpShape) -> int:
+    return lib().ep_check_shape(ctypes.byref(shape))
+
+
+def ep_num_nodes(shape: EpShape) -> int:
+    return lib().ep_num_nodes(ctypes.byref(shape))
+
+
+def ep_notify_workspace_bytes(shape: EpShape) -> int:
+    return int(lib().ep_notify_workspace_bytes(ctypes.byref(shape)))
+
+
+def ep_get_dispatch_layout(shape: EpShape, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                           num_tokens_per_expert, is_token_in_rank, status, stream=None) -> None:
+    R, T, K, E, N = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.num_experts, shape.N
+    rc = lib().ep_get_dispatch_layout(
+        ctypes.byref(shape), _t(topk_idx, torch.int64, (R, T, K), "topk_idx"),
+        _t(num_tokens_per_rank, torch.int32, (R, R), "num_tokens_per_rank"),
+        _t(num_tokens_per_rdma_rank, torch.int32, (R, N), "num_tokens_per_rdma_rank"),
+        _t(num_tokens_per_expert, torch.int32, (R, E), "num_tokens_per_expert"),
+        _t(is_token_in_rank, torch.uint8, (R, T, R), "is_token_in_rank"),
+        _t(status, torch.int32, (1,), "status"), _stream(stream))
+    _check("ep_get_dispatch_layout", rc)
+
+
+_NOTIFY_OUT = ("rank_prefix_matrix", "gbl_channel_prefix_matrix", "rdma_channel_prefix_matrix",
+               "recv_gbl_rank_prefix_sum", "recv_rdma_rank_prefix_sum", "recv_channel_offset",
+               "num_recv_tokens", "num_rdma_recv_tokens", "num_recv_tokens_per_expert", "recv_base",
+               "send_pos")
+
+
+def notify_shapes(shape: EpShape) -> dict:
+    R, T, C, N, El = shape.num_ranks, shape.num_tokens, shape.num_channels, shape.N, shape.E_loc
+    return dict(
+        rank_prefix_matrix=((R, R), torch.int32),
+        gbl_channel_prefix_matrix=((R, R, C), torch.int32),
+        rdma_channel_prefix_matrix=((R, N, C), torch.int32),
+        recv_gbl_rank_prefix_sum=((R, R), torch.int32),
+        recv_rdma_rank_prefix_sum=((R, N), torch.int32),
+        recv_channel_offset=((R, R, C), torch.int32),
+        num_recv_tokens=((R,), torch.int32),
+        num_rdma_recv_tokens=((R,), torch.int32),
+        num_recv_tokens_per_expert=((R, El), torch.int32),
+        recv_base=((R + 1,), torch.int64),
+        send_pos=((R, T, R), torch.int32),
+    )
+
+
+def _notify_args(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                 num_tokens_per_expert, outs: dict):
+    R, T, E, N = shape.num_ranks, shape.num_tokens, shape.num_experts, shape.N
+    shapes = notify_shapes(shape)
+    args = [_t(is_token_in_rank, torch.uint8, (R, T, R), "is_token_in_rank"),
+            _t(num_tokens_per_rank, torch.int32, (R, R), "num_tokens_per_rank"),
+            _t(num_tokens_per_rdma_rank, torch.int32, (R, N), "num_tokens_per_rdma_rank"),
+            _t(num_tokens_per_expert, torch.int32, (R, E), "num_tokens_per_expert")]
+    for k in _NOTIFY_OUT:
+        shp, dt = shapes[k]
+        args.append(_t(outs[k], dt, shp, k))
+    return args
+
+
+def ep_notify_dispatch(shape: EpShape, is_token_in_rank, num_tokens_per_rank,
+                       num_tokens_per_rdma_rank, num_tokens_per_expert, outs: dict, workspace,
+                       status, host_num_recv_tokens=None, stream=None) -> None:
+    """``outs`` maps each notify output name (see :func:`notify_shapes`) to its tensor.
+    ``host_num_recv_tokens`` may be a pinned, host-mapped int32 tensor of R+1."""
+    args = _notify_args(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                        num_tokens_per_expert, outs)
+    need = ep_notify_workspace_bytes(shape)
+    if workspace is None or not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    host = _vp(None)
+    if host_num_recv_tokens is not None:
+        if host_num_recv_tokens.dtype != torch.int32 or host_num_recv_tokens.numel() < shape.num_ranks + 1:
+            raise ValueError("host_num_recv_tokens must be int32 with R+1 elements")
+        host = _vp(host_num_recv_tokens.data_ptr())
+    rc = lib().ep_notify_dispatch(ctypes.byref(shape), *args, _vp(workspace.data_ptr()),
+                                  _sz(workspace.numel() * workspace.element_size()),
+                                  _t(status, torch.int32, (1,), "status"), host, _stream(stream))
+    _check("ep_notify_dispatch", rc)
+
+
+def ep_debug_notify_dispatch_stall(shape: EpShape, is_token_in_rank, num_tokens_per_rank,
+                                   num_tokens_per_rdma_rank, num_tokens_per_expert, outs: dict,
+                                   workspace, status, stall_block: int, wait_limit_us: int,
+                                   stream=None) -> None:
+    args = _notify_args(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                        num_tokens_per_expert, outs)
+    rc = lib().ep_debug_notify_dispatch_stall(
+        ctypes.byref(shape), *args, _vp(workspace.data_ptr()),
+        _sz(workspace.numel() * workspace.element_size()), _t(status, torch.int32, (1,), "status"),
+        _i32(stall_block), _i32(wait_limit_us), _stream(stream))
+    _check("ep_debug_notify_dispatch_stall", rc)
+
+
+def ep_dispatch(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x, recv_topk_idx,
+                recv_topk_w, recv_src_info, status, stream=None) -> None:
+    R, T, K, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.hidden
+    cap = _rows(recv_x, "recv_x")
+    rc = lib().ep_dispatch(
+        ctypes.byref(shape), _t(x, torch.bfloat16, (R, T, H), "x"),
+        _t(topk_idx, torch.int64, (R, T, K), "topk_idx"),
+        _t(topk_w, torch.float32, (R, T, K), "topk_w"),
+        _t(send_pos, torch.int32, (R, T, R), "send_pos"),
+        _t(recv_base, torch.int64, (R + 1,), "recv_base"), _i64(cap),
+        _t(recv_x, torch.bfloat16, (cap, H), "recv_x"),
+        _t(recv_topk_idx, torch.int64, (cap, K), "recv_topk_idx"),
+        _t(recv_topk_w, torch.float32, (cap, K), "recv_topk_w"),
+        _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info"),
+        _t(status, torch.int32, (1,), "status"), _stream(stream))
+    _check("ep_dispatch", rc)
+
+
+def ep_combine(shape: EpShape, y, y_w, send_pos, recv_base, combined_x, combined_w, status,
+               stream=None) -> None:
+    R, T, K, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.hidden
+    rows = _rows(y, "y")
+    rc = lib().ep_combine(
+        ctypes.byref(shape), _t(y, torch.bfloat16, (rows, H), "y"),
+        _t(y_w, torch.float32, (rows, K), "y_w", nullable=True), _i64(rows),
+        _t(send_pos, torch.int32, (R, T, R), "send_pos"),
+        _t(recv_base, torch.int64, (R + 1,), "recv_base"),
+        _t(combined_x, torch.bfloat16, (R, T, H), "combined_x"),
+        _t(combined_w, torch.float32, (R, T, K), "combined_w", nullable=True),
+        _t(status, torch.int32, (1,), "status"), _stream(stream))
+    _check("ep_combine", rc)
+
+
+def ep_sync_status(status, stream=None) -> int:
+    """Wait for the stream and return the status code the device word maps to."""
+    return int(lib().ep_sync_status(_t(status, torch.int32, (1,), "status"), _stream(stream)))
+
+
+# --------------------------------------------------------------------------- allocation
+def alloc_layout(shape: EpShape, device="cuda") -> dict:
+    R, T, E, N = shape.num_ranks, shape.num_tokens, shape.num_experts, shape.N
+    z = lambda *s, dt=torch.int32: torch.empty(s, dtype=dt, device=device)  # noqa: E731
+    return dict(num_tokens_per_rank=z(R, R), num_tokens_per_rdma_rank=z(R, N),
+                num_tokens_per_expert=z(R, E), is_token_in_rank=z(R, T, R, dt=torch.uint8))
+
+
+def alloc_notify(shape: EpShape, device="cuda") -> dict:
+    outs = {k: torch.empty(s, dtype=dt, device=device) for k, (s, dt) in notify_shapes(shape).items()}
+    ws = ep_notify_workspace_bytes(shape)
+    outs["workspace"] = torch.empty((ws + 15) // 16 * 16, dtype=torch.uint8, device=device)
+    return outs
+
+
+def alloc_dispatch(shape: EpShape, capacity_rows: int, device="cuda") -> dict:
+    H, K = shape.hidden, shape.num_topk
+    return dict(recv_x=torch.empty(capacity_rows, H, dtype=torch.bfloat16, device=device),
+                recv_topk_idx=torch.empty(capacity_rows, K, dtype=torch.int64, device=device),
+                recv_topk_w=torch.empty(capacity_rows, K, dtype=torch.float32, device=device),
+                recv_src_info=torch.empty(capacity_rows, 2, dtype=torch.int32, device=device))
+
+
+def alloc_combine(shape: EpShape, device="cuda") -> dict:
+    R, T, H, K = shape.num_ranks, shape.num_tokens, shape.hidden, shape.num_topk
+    return dict(combined_x=torch.empty(R, T, H, dtype=torch.bfloat16, device=device),
+                combined_w=torch.empty(R, T, K, dtype=torch.float32, device=device))
+
+
+@dataclass
+class Pipeline:
+    """Buffers for one shape plus the four calls in order (identity expert by
+    default).  Allocates once; :meth:`run` launches layout, notify, dispatch
+    and combine on the current stream without synchronising."""
+
+    shape: EpShape
+    capacity_rows: int
+    device: str = "cuda"
+
+    def __post_init__(self):
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.layout = alloc_layout(self.shape, self.device)
+        self.notify = alloc_notify(self.shape, self.device)
+        self.dispatch = alloc_dispatch(self.shape, self.capacity_rows, self.device)
+        self.combine = alloc_combine(self.shape, self.device)
+
+    def run(self, x, topk_idx, topk_w, y=None, y_w=None, stream=None, host_num_recv_tokens=None):
+        sh, L, Nt, D, C = self.shape, self.layout, self.notify, self.dispatch, self.combine
+        ep_get_dispatch_layout(sh, topk_idx, L["num_tokens_per_rank"], L["num_tokens_per_rdma_rank"],
+                               L["num_tokens_per_expert"], L["is_token_in_rank"], self.status, stream)
+        ep_notify_dispatch(sh, L["is_token_in_rank"], L["num_tokens_per_rank"],
+                           L["num_tokens_per_rdma_rank"], L["num_tokens_per_expert"], Nt,
+                           Nt["workspace"], self.status, host_num_recv_tokens, stream)
+        ep_dispatch(sh, x, topk_idx, topk_w, Nt["send_pos"], Nt["recv_base"], D["recv_x"],
+                    D["recv_topk_idx"], D["recv_topk_w"], D["recv_src_info"], self.status, stream)
+        ep_combine(sh, D["recv_x"] if y is None else y, D["recv_topk_w"] if y_w is None else y_w,
+                   Nt["send_pos"], Nt["recv_base"], C["combined_x"], C["combined_w"], self.status,
+                   stream)
+        return C["combined_x"], C["combined_w"]

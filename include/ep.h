@@ -1,0 +1,284 @@
+/*
+ * ep.h - C ABI of the GB300 (sm_103a) MoE expert-parallel dispatch/combine
+ * library (libep_gb300.so).
+ *
+ * The hot path has four steps, each one entry point below:
+ *   ep_get_dispatch_layout  count tokens per rank / node / expert and build
+ *                           is_token_in_rank from the router's top-k map
+ *   ep_notify_dispatch      prefix sums: rank and channel prefix matrices,
+ *                           receive counts and offsets, and the row map
+ *   ep_dispatch             copy every token row (and its top-k ids, weights
+ *                           and source info) into each destination's region
+ *   ep_combine              gather the rows back and sum them in fp32
+ *
+ * Pages the operations come from (cited by title and section):
+ *   [IN] "notify_dispatch (internode.cu)" notes on DeepEP: sm0 stages 3-6 and
+ *        sm1..x stages 1-3.
+ *   [CH] "cuda】deepep": channels as a partition of each rank's tokens.
+ *   [RT] mscclpp src/ext/ep/ht_runtime.cc: MoEHighThroughputRuntime::
+ *        getDispatchLayout, intranode/internodeNotifyDispatch,
+ *        intranode/internodeDispatch, intranode/internodeCombine.
+ *   [AR] "CUDA与DeepEP：分布式MoE系统中的高效通信机制解析": 2.2 rank-to-node
+ *        mapping, 3.2 reductions and prefix sums, 4.1 SrcInfo, 4.2 combine.
+ *
+ * Model.  R "ranks" are logical partitions of ONE GPU's memory.  Every
+ * rank-indexed array is stacked along a leading rank axis on the same device
+ * (x is [R][T][H], topk_idx is [R][T][K], ...).  Sending to rank r is a store
+ * into r's region of one receive pool; nothing crosses a GPU boundary.
+ *
+ * Notation: R ranks, N = max(1, R/8) nodes (node of rank r is r/8, [AR] 2.2),
+ * T tokens per rank, K top-k slots, E experts, E_loc = E/R experts per rank,
+ * H hidden size in bf16 elements, C channels.  Channel c of a rank holds its
+ * tokens [min(c*q, T), min((c+1)*q, T)) with q = ceil(T/C) ([CH]).
+ *
+ * Conventions for every call:
+ *   - All array arguments are DEVICE pointers (cudaMalloc / torch memory)
+ *     unless marked "host".  Arrays are dense, C-order, 16-byte aligned.
+ *   - The caller owns and allocates every buffer.  Apart from
+ *     ep_sync_status's 4-byte read-back, no call allocates, frees or keeps
+ *     state between calls.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and
+ *     return after enqueueing.  The host checks arguments first and returns
+ *     EP_ERR_INVALID_ARG without enqueueing anything when they are wrong.
+ *   - Errors found on the device (receive capacity exceeded, a wait that ran
+ *     out, inputs that disagree) are OR-ed as EP_DEV_* bits into the
+ *     caller's `status` word; the kernels never trap.  ep_sync_status turns
+ *     the word into an ep_status_t.  Zero the word before the first call.
+ *   - Outputs are a pure function of the inputs: re-running a call gives
+ *     byte-identical results (no atomics decide any output value).
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = -1,   /* a size, pointer or alignment rule is broken */
+    EP_ERR_CUDA = -2,          /* a CUDA runtime call failed */
+    EP_ERR_CAPACITY = -3,      /* receive pool smaller than the rows to place */
+    EP_ERR_TIMEOUT = -4,       /* a bounded device wait ran out */
+    EP_ERR_INCONSISTENT = -5,  /* count inputs disagree with is_token_in_rank */
+    EP_ERR_INPUT = -6          /* an expert id outside [-1, E) */
+} ep_status_t;
+
+/* Bits the kernels OR into the device status word. */
+#define EP_DEV_CAPACITY 0x1
+#define EP_DEV_TIMEOUT 0x2
+#define EP_DEV_INCONSISTENT 0x4
+#define EP_DEV_INPUT 0x8
+
+/* Problem shape.  Rules (EP_ERR_INVALID_ARG otherwise):
+ *   1 <= R <= 32, and R % 8 == 0 when R > 8 (whole nodes of 8 ranks);
+ *   T >= 0, R * T < 2^30;  1 <= K <= 32;  E >= R and E % R == 0, E <= 8192;
+ *   H >= 8 and H % 8 == 0 (rows are whole 16-byte vectors, [RT] asserts
+ *   (hidden * elem) % sizeof(int4) == 0);  1 <= C <= 4096;
+ *   expert_alignment >= 1. */
+typedef struct {
+    int32_t num_ranks;        /* R */
+    int32_t num_tokens;       /* T, tokens per source rank */
+    int32_t num_topk;         /* K */
+    int32_t num_experts;      /* E */
+    int32_t hidden;           /* H, bf16 elements per token row */
+    int32_t num_channels;     /* C */
+    int32_t expert_alignment; /* per-expert receive counts round up to this */
+} ep_shape_t;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* ep_status_string(ep_status_t status);
+
+/* EP_OK when `shape` obeys the rules above, else EP_ERR_INVALID_ARG. */
+ep_status_t ep_check_shape(const ep_shape_t* shape);
+
+/* Number of nodes N = max(1, R/8), or -1 for an invalid shape. */
+int32_t ep_num_nodes(const ep_shape_t* shape);
+
+/* Bytes of device scratch ep_notify_dispatch needs (its `workspace`), or 0
+ * for an invalid shape. */
+size_t ep_notify_workspace_bytes(const ep_shape_t* shape);
+
+/* ------------------------------------------------------------------------
+ * Step 1 - layout.  [RT] getDispatchLayout; the three count vectors are the
+ * ones [IN] sm0 stage 3 packs for each destination node.
+ *
+ *   topk_idx                 in   int64 [R][T][K]  expert id in [0,E), or -1
+ *                                                   for an empty slot
+ *   num_tokens_per_rank      out  int32 [R][R]     [s][r]: tokens of s with
+ *                                                   at least one expert on r
+ *   num_tokens_per_rdma_rank out  int32 [R][N]     [s][n]: tokens of s with
+ *                                                   an expert on node n
+ *   num_tokens_per_expert    out  int32 [R][E]     [s][e]: slots of s naming
+ *                                                   e (a repeated id counts
+ *                                                   every time)
+ *   is_token_in_rank         out  uint8 [R][T][R]  1 when token (s,t) has an
+ *                                                   expert on rank r, else 0
+ *   status                   in/out int32 device status word
+ * Expert e lives on rank e / E_loc.  An id outside [-1, E) sets EP_DEV_INPUT
+ * and is ignored.  Every output element is written (no pre-zeroing needed).
+ */
+ep_status_t ep_get_dispatch_layout(const ep_shape_t* shape, const int64_t* topk_idx,
+                                   int32_t* num_tokens_per_rank,
+                                   int32_t* num_tokens_per_rdma_rank,
+                                   int32_t* num_tokens_per_expert,
+                                   uint8_t* is_token_in_rank, int32_t* status,
+                                   cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 2 - notify.  [IN] sm1..x stages 1-3 (per-channel counts and their
+ * prefix) and sm0 stage 6 (per-rank prefix over global source rank, node
+ * prefix, per-expert totals rounded up to expert_alignment); [RT]
+ * intranodeNotifyDispatch / internodeNotifyDispatch for the outputs' names
+ * and shapes.  One single-pass decoupled-lookback scan over the R*C
+ * (source rank, channel) blocks.
+ *
+ * Inputs (as produced by step 1):
+ *   is_token_in_rank           uint8 [R][T][R]
+ *   num_tokens_per_rank        int32 [R][R]
+ *   num_tokens_per_rdma_rank   int32 [R][N]
+ *   num_tokens_per_expert      int32 [R][E]
+ * Outputs:
+ *   rank_prefix_matrix         int32 [R src][R dst]  sum over s' <= s of
+ *                                                     num_tokens_per_rank[s'][r]
+ *   gbl_channel_prefix_matrix  int32 [R src][R dst][C] tokens of s in
+ *                                                     channels <= c sent to r
+ *   rdma_channel_prefix_matrix int32 [R src][N][C]   same, per node
+ *   recv_gbl_rank_prefix_sum   int32 [R dst][R src]  transpose of
+ *                                                     rank_prefix_matrix
+ *   recv_rdma_rank_prefix_sum  int32 [R dst][N]      [r][m]: sum over m' <= m
+ *                                                     of what rank m'*8 + r%8
+ *                                                     sends to node r/8
+ *   recv_channel_offset        int32 [R dst][R src][C] first row of block
+ *                                                     (s,c) in r's region
+ *   num_recv_tokens            int32 [R]             rows rank r receives
+ *   num_rdma_recv_tokens       int32 [R]             last column of
+ *                                                     recv_rdma_rank_prefix_sum
+ *   num_recv_tokens_per_expert int32 [R][E_loc]      per local expert,
+ *                                                     rounded up to alignment
+ *   recv_base                  int64 [R+1]           region of rank r starts at
+ *                                                     pool row recv_base[r];
+ *                                                     recv_base[R] = total rows
+ *   send_pos                   int32 [R src][T][R dst] row of (s,t) inside r's
+ *                                                     region, or -1
+ *   workspace                  device scratch of ep_notify_workspace_bytes();
+ *                              cleared by this call, contents undefined after
+ *   host_num_recv_tokens       optional (may be NULL): int32 [R+1] in
+ *                              host-mapped pinned memory (cudaHostAlloc with
+ *                              cudaHostAllocMapped, or any device-visible
+ *                              pointer); receives num_recv_tokens and the
+ *                              total, so the host can size its buffers after a
+ *                              stream sync without another copy
+ * Rows of r's region are ordered by (source rank, channel, token), which is
+ * (source rank, token) order.  If the count inputs disagree with
+ * is_token_in_rank, EP_DEV_INCONSISTENT is set (the outputs then follow
+ * is_token_in_rank for the channel matrices and send_pos, and the count
+ * inputs for the rest).  A bounded wait that runs out sets EP_DEV_TIMEOUT.
+ */
+ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_in_rank,
+                               const int32_t* num_tokens_per_rank,
+                               const int32_t* num_tokens_per_rdma_rank,
+                               const int32_t* num_tokens_per_expert,
+                               int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+                               int32_t* rdma_channel_prefix_matrix,
+                               int32_t* recv_gbl_rank_prefix_sum,
+                               int32_t* recv_rdma_rank_prefix_sum, int32_t* recv_channel_offset,
+                               int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+                               int32_t* num_recv_tokens_per_expert, int64_t* recv_base,
+                               int32_t* send_pos, void* workspace, size_t workspace_bytes,
+                               int32_t* status, int32_t* host_num_recv_tokens,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 3 - dispatch.  [RT] intranodeDispatch / internodeDispatch (receive
+ * side: recv_x, recv_topk_idx, recv_topk_weights, source index), [AR] 4.1
+ * (SrcInfo {src_rank, src_idx}).  Token (s,t) is copied to pool row
+ * recv_base[r] + send_pos[s][t][r] for every r with send_pos >= 0.
+ *
+ *   x              in  bf16 bits (uint16) [R][T][H]
+ *   topk_idx       in  int64 [R][T][K]
+ *   topk_w         in  fp32  [R][T][K]
+ *   send_pos       in  int32 [R][T][R]   from ep_notify_dispatch
+ *   recv_base      in  int64 [R+1]       from ep_notify_dispatch (device)
+ *   capacity_rows  rows allocated in the four recv_* arrays; a row at or
+ *                  beyond it is not written and EP_DEV_CAPACITY is set.
+ *                  R*T*min(K,R) always suffices.
+ *   recv_x         out bf16 [capacity_rows][H]   bit copies of x rows
+ *   recv_topk_idx  out int64 [capacity_rows][K]  local expert id (e - r*E_loc)
+ *                      where expert e lives on the receiving rank r, else -1
+ *   recv_topk_w    out fp32 [capacity_rows][K]   the slot's weight where its
+ *                      expert lives on r, else 0
+ *   recv_src_info  out int32 [capacity_rows][2]  (source rank, source token)
+ * Rows beyond recv_base[R] are left untouched.
+ */
+ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
+                        const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
+                        int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                        float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                        cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 4 - combine.  [RT] intranodeCombine / internodeCombine (combined_x is
+ * bf16, combined_topk_weights fp32), [AR] 4.2 (each received row returns to
+ * its (src_rank, src_idx)).  For every source token (s,t):
+ *   combined_x[s][t][h] = bf16_rne( sum over r ascending with
+ *                          send_pos[s][t][r] >= 0 of float(y[recv_base[r] +
+ *                          send_pos[s][t][r]][h]) ), starting from +0.0f;
+ *   combined_w[s][t][k] = the same fp32 sum over y_w, not rounded.
+ * A token with no destination combines to +0.  The sum is unweighted (an
+ * expert applies its routing weights before combine).
+ *
+ *   y           in  bf16 bits [pool rows][H]  expert outputs, one per
+ *                   received row (recv_x itself for an identity expert);
+ *                   must be a valid array whenever R*T > 0
+ *   y_w         in  fp32 [pool rows][K]; may be NULL when combined_w is
+ *   y_rows      rows allocated in y (and y_w); a contribution whose row is
+ *               at or beyond it is skipped and EP_DEV_CAPACITY is set
+ *   send_pos    in  int32 [R][T][R]
+ *   recv_base   in  int64 [R+1] (device)
+ *   combined_x  out bf16 [R][T][H]
+ *   combined_w  out fp32 [R][T][K], or NULL to skip the weights
+ * Empty arrays (zero elements) may be passed as NULL in every call.
+ */
+ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* y_w,
+                       int64_t y_rows, const int32_t* send_pos, const int64_t* recv_base,
+                       uint16_t* combined_x, float* combined_w, int32_t* status,
+                       cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Waits for `stream`, reads the device status word (a 4-byte copy into host
+ * memory owned by this call), and maps its bits to a status: EP_OK,
+ * EP_ERR_TIMEOUT, EP_ERR_CAPACITY, EP_ERR_INPUT or EP_ERR_INCONSISTENT (in
+ * that priority), or EP_ERR_CUDA when the wait or copy fails.  The word is
+ * not cleared.
+ */
+ep_status_t ep_sync_status(const int32_t* status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Testing hook for failure detection.  Runs ep_notify_dispatch with the
+ * block at scan position `stall_block` withholding its published prefix and
+ * every wait bounded by `wait_limit_us` microseconds.  The blocks that wait
+ * on it give up, set EP_DEV_TIMEOUT and exit, so the context stays usable.
+ * Output contents are undefined after such a run.
+ */
+ep_status_t ep_debug_notify_dispatch_stall(
+    const ep_shape_t* shape, const uint8_t* is_token_in_rank,
+    const int32_t* num_tokens_per_rank, const int32_t* num_tokens_per_rdma_rank,
+    const int32_t* num_tokens_per_expert, int32_t* rank_prefix_matrix,
+    int32_t* gbl_channel_prefix_matrix, int32_t* rdma_channel_prefix_matrix,
+    int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+    int32_t* recv_channel_offset, int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+    int32_t* num_recv_tokens_per_expert, int64_t* recv_base, int32_t* send_pos, void* workspace,
+    size_t workspace_bytes, int32_t* status, int32_t stall_block, int32_t wait_limit_us,
+    cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */

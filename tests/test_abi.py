@@ -1,0 +1,115 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; host-side argument checks work without a GPU (no kernel runs)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ep.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def ep():
+    from combine_get_dispatch_notify_gb300 import build, ep as binding
+    build.build()
+    binding.lib()
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(ep):
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(ep.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ep.h but not exported"
+    assert sorted(ep.exported_symbols()) == names
+
+
+def test_library_links_against_the_shared_cuda_runtime(ep):
+    with open("/proc/self/maps") as f:
+        maps = f.read()
+    assert "libep_gb300.so" in maps
+
+
+def test_shape_rules(ep):
+    S = ep.EpShape.make
+    ok = [S(1, 5, 1, 1, 8, 1), S(2, 128, 2, 16, 256, 2), S(16, 128, 8, 256, 7168, 8),
+          S(32, 16384, 8, 256, 7168, 32), S(3, 0, 2, 9, 72, 5), S(8, 10, 32, 8192, 8, 4096)]
+    bad = [S(0, 5, 1, 1, 8, 1), S(12, 5, 1, 12, 8, 1), S(40, 5, 1, 40, 8, 1), S(2, 5, 0, 2, 8, 1),
+           S(2, 5, 33, 2, 8, 1), S(4, 5, 2, 6, 8, 1), S(4, 5, 2, 2, 8, 1), S(2, 5, 2, 4, 12, 1),
+           S(2, 5, 2, 4, 8, 0), S(2, -1, 2, 4, 8, 1), S(32, 1 << 25, 8, 256, 8, 1),
+           ep.EpShape(2, 5, 2, 4, 8, 1, 0), S(2, 5, 2, 4, 8, 4097)]
+    for s in ok:
+        assert ep.ep_check_shape(s) == ep.EP_OK, tuple(getattr(s, f) for f, _ in s._fields_)
+    for s in bad:
+        assert ep.ep_check_shape(s) == ep.EP_ERR_INVALID_ARG, tuple(getattr(s, f) for f, _ in s._fields_)
+
+
+def test_nodes_and_workspace(ep):
+    S = ep.EpShape.make
+    assert ep.ep_num_nodes(S(4, 8, 2, 8, 8, 2)) == 1
+    assert ep.ep_num_nodes(S(8, 8, 2, 8, 8, 2)) == 1
+    assert ep.ep_num_nodes(S(16, 8, 2, 16, 8, 2)) == 2
+    assert ep.ep_num_nodes(S(32, 8, 2, 32, 8, 2)) == 4
+    assert ep.ep_num_nodes(S(12, 8, 2, 12, 8, 2)) == -1
+    # one 8-byte lookback word per (block, rank or node), plus a header
+    s = S(16, 128, 8, 256, 7168, 8)
+    assert ep.ep_notify_workspace_bytes(s) == 256 + 16 * 8 * (16 + 2) * 8
+    assert ep.ep_notify_workspace_bytes(S(12, 8, 2, 12, 8, 2)) == 0
+
+
+def test_status_strings(ep):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert ep.ep_status_string(code) and ep.ep_status_string(code) != "unknown status"
+    assert ep.ep_status_string(7) == "unknown status"
+
+
+def test_invalid_calls_return_before_touching_the_device(ep):
+    """Bad shapes and NULL / misaligned pointers are refused on the host."""
+    vp = ctypes.c_void_p
+    good = ep.EpShape.make(2, 4, 2, 4, 8, 2)
+    badshape = ep.EpShape.make(12, 4, 2, 12, 8, 2)
+    fake = vp(1 << 20)        # aligned, never dereferenced: the call must fail first
+    odd = vp((1 << 20) + 4)   # misaligned for 16-byte arrays
+    L = ep.lib()
+    assert L.ep_get_dispatch_layout(ctypes.byref(badshape), fake, fake, fake, fake, fake, fake,
+                                    vp(0)) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_get_dispatch_layout(ctypes.byref(good), odd, fake, fake, fake, fake, fake,
+                                    vp(0)) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_get_dispatch_layout(ctypes.byref(good), vp(None), fake, fake, fake, fake, fake,
+                                    vp(0)) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch(ctypes.byref(good), fake, fake, fake, fake, fake, ctypes.c_int64(-1), fake,
+                         fake, fake, fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch(ctypes.byref(good), odd, fake, fake, fake, fake, ctypes.c_int64(8), fake,
+                         fake, fake, fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_combine(ctypes.byref(good), vp(None), vp(None), 4, fake, fake, fake, vp(None), fake,
+                        vp(0)) == ep.EP_ERR_INVALID_ARG  # y missing
+    assert L.ep_combine(ctypes.byref(good), fake, vp(None), 4, fake, fake, fake, fake, fake,
+                        vp(0)) == ep.EP_ERR_INVALID_ARG  # combined_w without y_w
+    assert L.ep_combine(ctypes.byref(good), fake, fake, -1, fake, fake, fake, fake, fake,
+                        vp(0)) == ep.EP_ERR_INVALID_ARG  # negative y_rows
+    args = [fake] * 16
+    assert L.ep_notify_dispatch(ctypes.byref(good), *args, ctypes.c_size_t(8), fake, vp(None),
+                                vp(0)) == ep.EP_ERR_INVALID_ARG  # workspace too small
+    assert L.ep_debug_notify_dispatch_stall(ctypes.byref(good), *args, ctypes.c_size_t(1 << 20), fake,
+                                            0, 0, vp(0)) == ep.EP_ERR_INVALID_ARG  # zero wait limit
+
+
+def test_binding_refuses_cpu_tensors(ep):
+    s = ep.EpShape.make(2, 4, 2, 4, 8, 2)
+    t = torch.zeros(2, 4, 2, dtype=torch.int64)
+    with pytest.raises(ValueError):
+        ep.ep_get_dispatch_layout(s, t, None, None, None, None, None)

@@ -1,0 +1,293 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+* small workloads (tiny, low_latency, prefill) and edge shapes: every output
+  of every step compared with the oracle (integers and bytes bit-exact,
+  combine within |d| <= 1e-2 + 8e-3|ref| and bit-exact);
+* full-size workloads (skewed, large): layout, notify and all dispatch
+  metadata compared in full; the dispatched payload checked at full size by
+  the property recv_x[p] == x[src_info[p]] plus oracle rows on a sample;
+  combine checked at full size by the identity-expert closed form and, for
+  random expert outputs, against the oracle on a sample of tokens.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_get_dispatch_notify_gb300 import ep
+from combine_get_dispatch_notify_gb300.workloads import CONFIGS, Workload, worst_case_rows
+from gpu_util import (assert_combine_close, assert_equal, check_layout_notify, make_inputs,
+                      run_layout_notify, shape_of, u16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ep.lib()
+
+
+def full_parity(w: Workload, random_expert: bool = True, capacity: int | None = None):
+    """Run all four steps and compare every output with the oracle."""
+    o = oracle.load()
+    idx, wt, x = make_inputs(w)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    lay, nt, dp, cb = oracle.run_all(w.R, w.T, w.K, w.E, w.H, w.C, w.expert_alignment, xb,
+                                     idx.numpy(), wt.numpy(), o)
+    rows = int(nt["recv_base"][-1])
+    sh = shape_of(w)
+    pipe = ep.Pipeline(sh, capacity if capacity is not None else max(1, worst_case_rows(w)))
+    cx, cw = pipe.run(x.cuda(), idx.cuda(), wt.cuda())
+    assert ep.ep_sync_status(pipe.status) == ep.EP_OK
+    check_layout_notify(pipe.layout, pipe.notify, lay, nt)
+    D = pipe.dispatch
+    assert_equal("recv_x", u16(D["recv_x"][:rows]), dp["recv_x"])
+    assert_equal("recv_topk_idx", D["recv_topk_idx"][:rows].cpu().numpy(), dp["recv_topk_idx"])
+    assert_equal("recv_topk_w", D["recv_topk_w"][:rows].cpu().numpy(), dp["recv_topk_w"])
+    assert_equal("recv_src_info", D["recv_src_info"][:rows].cpu().numpy(), dp["recv_src_info"])
+    assert_combine_close("combined_x", u16(cx), cb["combined_x"])
+    assert_equal("combined_w", cw.cpu().numpy(), cb["combined_w"])
+
+    # a second run gives byte-identical results
+    snap = {k: v.clone() for k, v in pipe.notify.items() if k != "workspace"}
+    snap_cx = cx.clone()
+    pipe.run(x.cuda(), idx.cuda(), wt.cuda())
+    assert ep.ep_sync_status(pipe.status) == ep.EP_OK
+    for k, v in snap.items():
+        assert torch.equal(v, pipe.notify[k]), f"{k} differs between runs"
+    assert torch.equal(snap_cx.view(torch.int16), cx.view(torch.int16))
+
+    if random_expert and rows > 0:
+        # an expert whose outputs differ per row: order of the sum matters
+        g = torch.Generator().manual_seed(1234)
+        y = (torch.randn(rows, w.H, generator=g) * 3).to(torch.bfloat16)
+        yw = torch.randn(rows, w.K, generator=g)
+        ref = o.combine(w.R, w.T, w.K, w.H, y.view(torch.int16).numpy().view(np.uint16), yw.numpy(),
+                        nt["send_pos"], nt["recv_base"])
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = ep.alloc_combine(sh)
+        ep.ep_combine(sh, y.cuda(), yw.cuda(), pipe.notify["send_pos"], pipe.notify["recv_base"],
+                      out["combined_x"], out["combined_w"], status)
+        assert ep.ep_sync_status(status) == ep.EP_OK
+        assert_combine_close("combined_x (random expert)", u16(out["combined_x"]), ref["combined_x"])
+        assert_equal("combined_w (random expert)", out["combined_w"].cpu().numpy(), ref["combined_w"])
+    return pipe
+
+
+@pytest.mark.parametrize("name", ["tiny", "low_latency", "prefill"])
+def test_workload_full_parity(name):
+    full_parity(CONFIGS[name])
+
+
+EDGE = {
+    "single_rank": Workload("e", R=1, T=37, H=64, E=6, K=3, C=4, routing="replace", mask=0.2),
+    "empty_tokens": Workload("e", R=4, T=0, H=64, E=8, K=2, C=3),
+    "channels_exceed_tokens": Workload("e", R=8, T=50, H=128, E=64, K=4, C=64, mask=0.1),
+    "top1_counting_sort": Workload("e", R=16, T=33, H=256, E=64, K=1, C=5),
+    "r32_min_hidden_repeats": Workload("e", R=32, T=19, H=8, E=256, K=8, C=3, routing="replace",
+                                       mask=0.3),
+    "all_masked": Workload("e", R=8, T=40, H=64, E=16, K=4, C=4, mask=1.0),
+    "ragged_hidden": Workload("e", R=4, T=70, H=264, E=8, K=3, C=7, routing="zipf"),
+    "odd_ranks_align": Workload("e", R=3, T=41, H=72, E=9, K=2, C=5, expert_alignment=4),
+    "align128": Workload("e", R=16, T=64, H=512, E=128, K=8, C=6, expert_alignment=128),
+    "odd_topk": Workload("e", R=8, T=29, H=1024, E=32, K=5, C=2, mask=0.15),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EDGE))
+def test_edge_parity(case):
+    full_parity(EDGE[case])
+
+
+def _sample_tokens(R, T, n, seed):
+    rng = np.random.default_rng(seed)
+    g = rng.choice(R * T, size=min(n, R * T), replace=False)
+    return np.sort(g)
+
+
+@pytest.mark.parametrize("name", ["skewed", "large"])
+def test_workload_full_size(name):
+    """Full-size layout/notify/metadata parity, payload property + sampled rows,
+    combine closed form + sampled oracle tokens."""
+    w = CONFIGS[name]
+    o = oracle.load()
+    idx, wt, x = make_inputs(w, x_on_gpu=True)
+    lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+    nt_ref = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref)
+    rows = int(nt_ref["recv_base"][-1])
+    sh = shape_of(w)
+    pipe = ep.Pipeline(sh, rows)
+    cx, cw = pipe.run(x, idx.cuda(), wt.cuda())
+    assert ep.ep_sync_status(pipe.status) == ep.EP_OK
+    check_layout_notify(pipe.layout, pipe.notify, lay_ref, nt_ref)
+
+    # dispatch metadata in full
+    dp_ref = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, None, idx.numpy(), wt.numpy(),
+                        nt_ref["send_pos"], nt_ref["recv_base"], payload=False)
+    D = pipe.dispatch
+    src = D["recv_src_info"].cpu().numpy()
+    assert_equal("recv_src_info", src, dp_ref["recv_src_info"])
+    assert_equal("recv_topk_idx", D["recv_topk_idx"].cpu().numpy(), dp_ref["recv_topk_idx"])
+    assert_equal("recv_topk_w", D["recv_topk_w"].cpu().numpy(), dp_ref["recv_topk_w"])
+
+    # payload: every row is a bit copy of its source row (full size, on device)
+    xf = x.view(torch.int16).view(-1, w.H)
+    src_g = torch.from_numpy(src[:, 0].astype(np.int64) * w.T + src[:, 1]).cuda()
+    rx = D["recv_x"].view(torch.int16)
+    for a in range(0, rows, 1 << 18):
+        b = min(rows, a + (1 << 18))
+        assert torch.equal(rx[a:b], xf[src_g[a:b]]), f"recv_x rows {a}..{b} differ from their source"
+    # payload: oracle dispatch of a sample of rows
+    pick = np.random.default_rng(5).choice(rows, size=min(rows, 2000), replace=False)
+    want = xf[src_g[torch.from_numpy(pick).cuda()]].cpu().numpy().view(np.uint16)
+    assert_equal("recv_x sample", rx[torch.from_numpy(pick).cuda()].cpu().numpy().view(np.uint16), want)
+
+    # combine, identity expert, full size: bf16(n_dest * x); +0 without destination
+    n_dest = (pipe.notify["send_pos"] >= 0).sum(-1).view(-1)
+    cxf = cx.view(-1, w.H)
+    for a in range(0, w.R * w.T, 1 << 16):
+        b = min(w.R * w.T, a + (1 << 16))
+        n = n_dest[a:b].to(torch.float32)[:, None]
+        exp = (x.view(-1, w.H)[a:b].float() * n).to(torch.bfloat16)
+        exp = torch.where(n == 0, torch.zeros_like(exp), exp)
+        assert torch.equal(cxf[a:b].view(torch.int16), exp.view(torch.int16)), f"combined rows {a}..{b}"
+    tw = wt.cuda()
+    assert torch.equal(cw, torch.where(idx.cuda() >= 0, tw, torch.zeros_like(tw))), "combined_w"
+
+    # combine, random expert outputs, oracle on sampled tokens
+    gen = torch.Generator(device="cuda").manual_seed(77)
+    for a in range(0, rows, 1 << 18):
+        b = min(rows, a + (1 << 18))
+        D["recv_x"][a:b].copy_(torch.randn(b - a, w.H, generator=gen, device="cuda") * 3)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_combine(sh, D["recv_x"], D["recv_topk_w"], pipe.notify["send_pos"], pipe.notify["recv_base"],
+                  cx, cw, status)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    toks = _sample_tokens(w.R, w.T, 1024, 9)
+    sp = nt_ref["send_pos"].reshape(-1, w.R)[toks]          # [n, R]
+    base = nt_ref["recv_base"]
+    rows_needed = [int(base[r] + sp[i, r]) for i in range(len(toks)) for r in range(w.R) if sp[i, r] >= 0]
+    y_small = D["recv_x"][torch.tensor(rows_needed, device="cuda")].view(torch.int16).cpu().numpy().view(np.uint16)
+    yw_small = D["recv_topk_w"][torch.tensor(rows_needed, device="cuda")].cpu().numpy()
+    # sub-problem: the sampled tokens as source rank 0, their rows numbered 0.. in order
+    sub_sp = -np.ones((w.R, len(toks), w.R), np.int32)
+    k = 0
+    for i in range(len(toks)):
+        for r in range(w.R):
+            if sp[i, r] >= 0:
+                sub_sp[0, i, r] = k
+                k += 1
+    ref = o.combine(w.R, len(toks), w.K, w.H, y_small, yw_small, sub_sp, np.zeros(w.R + 1, np.int64))
+    got = cx.view(-1, w.H)[torch.from_numpy(toks).cuda()]
+    assert_combine_close("combined_x sample (random expert)", u16(got), ref["combined_x"][0])
+    assert_equal("combined_w sample", cw.view(-1, w.K)[torch.from_numpy(toks).cuda()].cpu().numpy(),
+                 ref["combined_w"][0])
+
+
+# ---------------------------------------------------------------------------- errors
+def test_capacity_overflow_reports_status():
+    w = CONFIGS["tiny"]
+    idx, wt, x = make_inputs(w)
+    o = oracle.load()
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    lay, nt, dp, cb = oracle.run_all(w.R, w.T, w.K, w.E, w.H, w.C, 1, xb, idx.numpy(), wt.numpy(), o)
+    rows = int(nt["recv_base"][-1])
+    cap = rows // 2
+    pipe = ep.Pipeline(shape_of(w), cap)
+    pipe.run(x.cuda(), idx.cuda(), wt.cuda())
+    assert ep.ep_sync_status(pipe.status) == ep.EP_ERR_CAPACITY
+    # rows that fit are still exact
+    assert_equal("recv_x within capacity", u16(pipe.dispatch["recv_x"]), dp["recv_x"][:cap])
+    assert_equal("recv_src_info within capacity", pipe.dispatch["recv_src_info"].cpu().numpy(),
+                 dp["recv_src_info"][:cap])
+
+
+def test_bad_expert_id_reports_status():
+    w = CONFIGS["tiny"]
+    idx, wt, x = make_inputs(w)
+    idx = idx.clone()
+    idx[1, 5, 0] = w.E + 3
+    sh, lay, nt, status = run_layout_notify(w, idx)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_INPUT
+
+
+def test_inconsistent_counts_report_status():
+    w = CONFIGS["low_latency"]
+    idx, wt, x = make_inputs(w)
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay = ep.alloc_layout(sh)
+    nt = ep.alloc_notify(sh)
+    ep.ep_get_dispatch_layout(sh, idx.cuda(), lay["num_tokens_per_rank"], lay["num_tokens_per_rdma_rank"],
+                              lay["num_tokens_per_expert"], lay["is_token_in_rank"], status)
+    lay["num_tokens_per_rank"][3, 5] += 1
+    ep.ep_notify_dispatch(sh, lay["is_token_in_rank"], lay["num_tokens_per_rank"],
+                          lay["num_tokens_per_rdma_rank"], lay["num_tokens_per_expert"], nt,
+                          nt["workspace"], status)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_INCONSISTENT
+
+
+def test_stalled_lookback_times_out_and_context_survives():
+    """A block that never publishes: waiting blocks give up after the limit,
+    report EP_ERR_TIMEOUT, and the next normal run is correct."""
+    w = CONFIGS["low_latency"]
+    idx, wt, x = make_inputs(w)
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay = ep.alloc_layout(sh)
+    nt = ep.alloc_notify(sh)
+    ep.ep_get_dispatch_layout(sh, idx.cuda(), lay["num_tokens_per_rank"], lay["num_tokens_per_rdma_rank"],
+                              lay["num_tokens_per_expert"], lay["is_token_in_rank"], status)
+    ep.ep_debug_notify_dispatch_stall(sh, lay["is_token_in_rank"], lay["num_tokens_per_rank"],
+                                      lay["num_tokens_per_rdma_rank"], lay["num_tokens_per_expert"], nt,
+                                      nt["workspace"], status, stall_block=5, wait_limit_us=2000)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_TIMEOUT
+    # the context is still usable: a normal run matches the oracle
+    full_parity(CONFIGS["tiny"], random_expert=False)
+
+
+def test_invalid_arguments_rejected_on_host():
+    w = CONFIGS["tiny"]
+    idx, wt, x = make_inputs(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad = ep.EpShape.make(12, 16, 2, 24, 256, 2)  # 12 ranks: not whole nodes
+    lay = ep.alloc_layout(ep.EpShape.make(2, 16, 2, 24, 256, 2))
+    rc = ep.lib().ep_get_dispatch_layout(
+        __import__("ctypes").byref(bad), ep._vp(idx.cuda().data_ptr()),
+        ep._vp(lay["num_tokens_per_rank"].data_ptr()), ep._vp(lay["num_tokens_per_rdma_rank"].data_ptr()),
+        ep._vp(lay["num_tokens_per_expert"].data_ptr()), ep._vp(lay["is_token_in_rank"].data_ptr()),
+        ep._vp(status.data_ptr()), ep._vp(0))
+    assert rc == ep.EP_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        ep.ep_get_dispatch_layout(shape_of(w), idx, *[None] * 4, status)  # CPU tensor
+    with pytest.raises(ep.EpError):
+        sh = shape_of(w)
+        misaligned = torch.empty(w.R * w.T * w.K + 1, dtype=torch.int64, device="cuda")[1:].view(w.R, w.T, w.K)
+        L = ep.alloc_layout(sh)
+        ep.ep_get_dispatch_layout(sh, misaligned, L["num_tokens_per_rank"], L["num_tokens_per_rdma_rank"],
+                                  L["num_tokens_per_expert"], L["is_token_in_rank"], status)
+
+
+def test_host_mapped_receive_counts():
+    """notify can publish the receive counts into host-mapped pinned memory."""
+    w = CONFIGS["low_latency"]
+    idx, wt, x = make_inputs(w)
+    o = oracle.load()
+    nt_ref = o.notify(w.R, w.T, w.E, w.C, 1, o.layout(w.R, w.T, w.K, w.E, idx.numpy()))
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay = ep.alloc_layout(sh)
+    nt = ep.alloc_notify(sh)
+    host = torch.full((w.R + 1,), -1, dtype=torch.int32).pin_memory()
+    ep.ep_get_dispatch_layout(sh, idx.cuda(), lay["num_tokens_per_rank"], lay["num_tokens_per_rdma_rank"],
+                              lay["num_tokens_per_expert"], lay["is_token_in_rank"], status)
+    ep.ep_notify_dispatch(sh, lay["is_token_in_rank"], lay["num_tokens_per_rank"],
+                          lay["num_tokens_per_rdma_rank"], lay["num_tokens_per_expert"], nt,
+                          nt["workspace"], status, host_num_recv_tokens=host)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    want = np.concatenate([nt_ref["num_recv_tokens"], [nt_ref["recv_base"][-1]]]).astype(np.int32)
+    assert_equal("host_num_recv_tokens", host.numpy(), want)
