@@ -1,0 +1,472 @@
+"""Benchmark: one step = layout -> notify -> dispatch -> combine (identity
+expert) over one batch of a synthetic workload, through the C ABI.
+
+Prints ONE JSON line (rank 0).  Default workload: the low-latency shape
+(R=16 logical ranks, T=128 tokens/rank, H=7168, top-8 of 256 experts, C=8),
+the shape the dispatch/combine pages quote their latencies on.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+value   = algorithmic HBM bytes of the step / device time of the step (GB/s),
+          inputs resident in HBM, L2 flushed (256 MB write) before every step;
+e2e     = the same bytes / time of the step done end to end from pinned host
+          buffers (H2D of x, top-k ids and weights; D2H of the combined rows
+          and weights) through the same C-ABI calls;
+roofline: the dominant kernel (dispatch or combine) against the measured HBM
+          copy bandwidth;
+cpu_baseline: the CPU oracle on the same workload (single thread).
+With N > 1 (torchrun) every rank runs its own replica on its own GPU
+(replicas only: the path has no cross-GPU exchange on one node here);
+value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_get_dispatch_notify_gb300.workloads import (CONFIGS, describe, gen_routing,  # noqa: E402
+                                                         gen_x, worst_case_rows)
+
+METRIC = "dispatch/combine HBM GB/s, µs & tokens/s (H=7168, top-8, 256 experts), 1×GB300"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = {
+    "layout": "combine_get_dispatch_notify_gb300/csrc/layout.cu",
+    "notify": "combine_get_dispatch_notify_gb300/csrc/notify.cu",
+    "dispatch": "combine_get_dispatch_notify_gb300/csrc/dispatch.cu",
+    "combine": "combine_get_dispatch_notify_gb300/csrc/combine.cu",
+}
+
+
+# ----------------------------------------------------------------------------- bytes
+def algorithmic_bytes(w, P: int) -> dict:
+    """Bytes each step must read + write at least once (P = rows dispatched).
+
+    layout   R*T*8K  (top-k ids)          + R*T*R   (is_token_in_rank)
+    notify   R*T*R   (is_token_in_rank)   + R*T*R*4 (row map)
+    dispatch R*T*(2H + 12K) (x, ids, weights) + P*(2H + 12K + 8) (rows, ids,
+             weights, source info)
+    combine  P*(2H + 4K + 4) (rows, weights, row map) + R*T*(2H + 4K)
+    """
+    R, T, H, K = w.R, w.T, w.H, w.K
+    tok = R * T
+    return {
+        "layout": tok * 8 * K + tok * R,
+        "notify": tok * R + tok * R * 4,
+        "dispatch": tok * (2 * H + 12 * K) + P * (2 * H + 12 * K + 8),
+        "combine": P * (2 * H + 4 * K + 4) + tok * (2 * H + 4 * K),
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_digest(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it still matches the source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+        rec = table[kernel][workload]
+        if rec.get("source_sha256_16") != source_digest(KERNEL_SOURCES[kernel]):
+            return None
+        return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1:
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- dist
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return rank, local, world, dist
+    return 0, 0, 1, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_step_sample(w, budget_s: float, max_reps: int | None = None):
+    """Time the CPU oracle on the workload; returns (seconds per step, reps, P, note)."""
+    import oracle
+
+    o = oracle.load()
+    idx, wt = gen_routing(w)
+    x = gen_x(w).view(torch.int16).numpy().view(np.uint16)
+    idx_np, wt_np = idx.numpy(), wt.numpy()
+    times = []
+    P = 0
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        lay, nt, dp, cb = oracle.run_all(w.R, w.T, w.K, w.E, w.H, w.C, w.expert_alignment, x, idx_np,
+                                         wt_np, o)
+        times.append(time.perf_counter() - t0)
+        P = int(nt["recv_base"][-1])
+        if time.perf_counter() - t_start >= budget_s or (max_reps and len(times) >= max_reps):
+            break
+    return statistics.mean(times), len(times), P
+
+
+def run_reference(args, w):
+    rank, local, world, dist = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    budget = max(2.0, min(60.0, args.cpu_budget))
+    sec = []
+    P = 0
+    for _ in range(args.warmup):
+        oracle_step_sample(w, 0.0, max_reps=1)
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        s, reps, P = oracle_step_sample(w, 0.0, max_reps=1)
+        sec.append(s)
+        if time.perf_counter() - t_all > budget * 4:
+            break
+    step_s = statistics.mean(sec)
+    b = sum(algorithmic_bytes(w, P).values())
+    value = b / step_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": 1, "steps": len(sec), "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(w),
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"whole {w.name} workload per step (all {w.R * w.T} tokens), "
+                                   f"single-threaded C oracle, {len(sec)} steps"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    return {"workload": describe(w), "R": w.R, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "C": w.C,
+            "routing": w.routing, "mask": w.mask, "seed": w.seed,
+            "l2": "flushed before every step (256 MB device write)"}
+
+
+# ----------------------------------------------------------------------------- our arm
+class Step:
+    """The four C-ABI calls with arguments marshalled once (ctypes, device pointers)."""
+
+    def __init__(self, ep, pipe, x, idx, wt, stream):
+        import ctypes
+        self.ep = ep
+        self.L = ep.lib()
+        sh = pipe.shape
+        self.sh = ctypes.byref(sh)
+        v = ep._vp
+        p = lambda t: v(t.data_ptr())  # noqa: E731
+        La, Nt, D, C = pipe.layout, pipe.notify, pipe.dispatch, pipe.combine
+        s = v(stream.cuda_stream)
+        st = p(pipe.status)
+        self.layout_args = (self.sh, p(idx), p(La["num_tokens_per_rank"]), p(La["num_tokens_per_rdma_rank"]),
+                            p(La["num_tokens_per_expert"]), p(La["is_token_in_rank"]), st, s)
+        self.notify_args = (self.sh, p(La["is_token_in_rank"]), p(La["num_tokens_per_rank"]),
+                            p(La["num_tokens_per_rdma_rank"]), p(La["num_tokens_per_expert"]),
+                            *[p(Nt[k]) for k in ep._NOTIFY_OUT], p(Nt["workspace"]),
+                            ep._sz(Nt["workspace"].numel()), st, v(None), s)
+        cap = D["recv_x"].shape[0]
+        self.dispatch_args = (self.sh, p(x), p(idx), p(wt), p(Nt["send_pos"]), p(Nt["recv_base"]),
+                              ep._i64(cap), p(D["recv_x"]), p(D["recv_topk_idx"]), p(D["recv_topk_w"]),
+                              p(D["recv_src_info"]), st, s)
+        self.combine_args = (self.sh, p(D["recv_x"]), p(D["recv_topk_w"]), ep._i64(cap), p(Nt["send_pos"]),
+                             p(Nt["recv_base"]), p(C["combined_x"]), p(C["combined_w"]), st, s)
+
+    def layout(self):
+        rc = self.L.ep_get_dispatch_layout(*self.layout_args)
+        assert rc == 0, rc
+
+    def notify(self):
+        rc = self.L.ep_notify_dispatch(*self.notify_args)
+        assert rc == 0, rc
+
+    def dispatch(self):
+        rc = self.L.ep_dispatch(*self.dispatch_args)
+        assert rc == 0, rc
+
+    def combine(self):
+        rc = self.L.ep_combine(*self.combine_args)
+        assert rc == 0, rc
+
+    def all(self):
+        self.layout()
+        self.notify()
+        self.dispatch()
+        self.combine()
+
+
+def run_ours(args, w):
+    rank, local, world, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from combine_get_dispatch_notify_gb300 import ep
+
+    ep.lib()
+    sh = ep.EpShape.make(w.R, w.T, w.K, w.E, w.H, w.C, w.expert_alignment)
+    idx_h, wt_h = gen_routing(w)
+    x_d = gen_x(w, dev)
+    idx_d, wt_d = idx_h.to(dev), wt_h.to(dev)
+    pipe = ep.Pipeline(sh, worst_case_rows(w), str(dev))
+    stream = torch.cuda.current_stream(dev)
+    step = Step(ep, pipe, x_d, idx_d, wt_d, stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # correctness guard for the timed configuration (status word, rows placed)
+    step.all()
+    assert ep.ep_sync_status(pipe.status) == ep.EP_OK, "device status not OK"
+    P = int(pipe.notify["recv_base"][-1].item())
+    nbytes = algorithmic_bytes(w, P)
+    step_bytes = sum(nbytes.values())
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step.all()
+    torch.cuda.synchronize(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    with sampler:
+        # keep the GPU busy for the sampler before and after the timed region
+        pad_end = time.time() + 0.4
+        while time.time() < pad_end:
+            flush.fill_(1)
+            step.all()
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        for i in range(args.steps):
+            flush.fill_(1)
+            e = ev[i]
+            e[0].record(stream)
+            step.layout()
+            e[1].record(stream)
+            step.notify()
+            e[2].record(stream)
+            step.dispatch()
+            e[3].record(stream)
+            step.combine()
+            e[4].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+        t1 = time.time()
+        pad_end = time.time() + 0.4
+        while time.time() < pad_end:
+            flush.fill_(1)
+            step.all()
+        torch.cuda.synchronize(dev)
+    clocks = sampler.summary(t0 - 0.45, t1 + 0.45)
+    assert ep.ep_sync_status(pipe.status) == ep.EP_OK, "device status not OK after timing"
+
+    per = {k: [] for k in ("layout", "notify", "dispatch", "combine")}
+    steps_ms = []
+    for e in ev:
+        steps_ms.append(e[0].elapsed_time(e[4]))
+        for j, k in enumerate(per):
+            per[k].append(e[j].elapsed_time(e[j + 1]))
+    ms_local = statistics.mean(steps_ms)
+    ms = max_over_ranks(dist, ms_local)
+    total_bytes = sum_over_ranks(dist, step_bytes)
+    value = total_bytes / (ms * 1e-3) / 1e9
+
+    # end to end: pinned host inputs -> device -> the four calls -> host outputs
+    x_h = x_d.cpu().pin_memory()
+    idx_hp, wt_hp = idx_h.pin_memory(), wt_h.pin_memory()
+    cx_h = torch.empty_like(pipe.combine["combined_x"], device="cpu").pin_memory()
+    cw_h = torch.empty_like(pipe.combine["combined_w"], device="cpu").pin_memory()
+    h2d = x_h.numel() * 2 + idx_hp.numel() * 8 + wt_hp.numel() * 4
+    d2h = cx_h.numel() * 2 + cw_h.numel() * 4
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        idx_d.copy_(idx_hp, non_blocking=True)
+        wt_d.copy_(wt_hp, non_blocking=True)
+        step.all()
+        cx_h.copy_(pipe.combine["combined_x"], non_blocking=True)
+        cw_h.copy_(pipe.combine["combined_w"], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_ms_max = max_over_ranks(dist, statistics.mean(e2e_ms))
+    e2e_value = total_bytes / (e2e_ms_max * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    dom = max(("dispatch", "combine"), key=lambda k: statistics.mean(per[k]))
+    dom_ms = statistics.mean(per[dom])
+    achieved = nbytes[dom] / (dom_ms * 1e-3) / 1e9
+    tokens = w.R * w.T
+    per_op = {}
+    for k, vals in per.items():
+        m = statistics.mean(vals)
+        per_op[k] = {"us": round(m * 1e3, 2), "us_median": round(statistics.median(vals) * 1e3, 2),
+                     "GB_per_s": round(nbytes[k] / (m * 1e-3) / 1e9, 1),
+                     "tokens_per_s": round(tokens / (m * 1e-3), 1),
+                     "frac_of_hbm": round(nbytes[k] / (m * 1e-3) / 1e9 / peak, 4),
+                     "algorithmic_bytes": nbytes[k]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        sec, reps, _ = oracle_step_sample(w, args.cpu_budget)
+        cpu = {"value": round(step_bytes / sec / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"whole {w.name} workload ({tokens} tokens, all four steps) repeated "
+                         f"{reps}x, single-threaded C oracle",
+               "ms_per_step": round(sec * 1e3, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_dict(w),
+            "tokens_per_s": round(tokens * world / (ms * 1e-3), 1),
+            "rows_dispatched": P,
+            "per_op": per_op,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": recorded_traffic(dom, w.name),
+                         "algorithmic_bytes_per_launch": nbytes[dom]},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4)},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="low_latency", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work to time")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
