@@ -160,9 +160,9 @@ def test_workload_full_size(name):
 
     # combine, random expert outputs, oracle on sampled tokens
     gen = torch.Generator(device="cuda").manual_seed(77)
-    for a in range(0, rows, 1 << 18):
-        b = min(rows, a + (1 << 18))
-        D["recv_x"][a:b].copy_(torch.randn(b - a, w.H, generator=gen, device="cuda") * 3)
+    for a in range(0, rows, 1 << 16):
+        b = min(rows, a + (1 << 16))
+        D["recv_x"][a:b].copy_(torch.randn(b - a, w.H, generator=gen, device="cuda").mul_(3))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ep.ep_combine(sh, D["recv_x"], D["recv_topk_w"], pipe.notify["send_pos"], pipe.notify["recv_base"],
                   cx, cw, status)
