@@ -170,6 +170,30 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
                              ep::kDefaultWaitLimitNs, stream);
 }
 
+ep_status_t ep_notify_dispatch_noalloc(
+    const ep_shape_t* shape, const uint8_t* is_token_in_rank, const int32_t* num_tokens_per_rank,
+    const int32_t* num_tokens_per_rdma_rank, const int32_t* num_tokens_per_expert,
+    int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+    int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum,
+    int32_t* recv_rdma_rank_prefix_sum, int32_t* recv_channel_offset, int32_t* num_recv_tokens,
+    int32_t* num_rdma_recv_tokens, int32_t* num_recv_tokens_per_expert, int64_t* recv_base,
+    int32_t* send_pos, int32_t* status, int32_t* host_num_recv_tokens, cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    // The shape must fit the fixed scratch; larger shapes are refused here,
+    // before anything is enqueued.
+    if (ep::notify_workspace_bytes(sh) > ep::kNoAllocScratchBytes) return EP_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    if (ep::notify_noalloc_scratch(&scratch) != cudaSuccess) return EP_ERR_CUDA;
+    return ep::notify_common(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                             num_tokens_per_expert, rank_prefix_matrix, gbl_channel_prefix_matrix,
+                             rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
+                             recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
+                             num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos,
+                             scratch, ep::kNoAllocScratchBytes, status, host_num_recv_tokens, -1,
+                             ep::kDefaultWaitLimitNs, stream);
+}
+
 ep_status_t ep_debug_notify_dispatch_stall(
     const ep_shape_t* shape, const uint8_t* is_token_in_rank, const int32_t* num_tokens_per_rank,
     const int32_t* num_tokens_per_rdma_rank, const int32_t* num_tokens_per_expert,

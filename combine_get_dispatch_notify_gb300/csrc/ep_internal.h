@@ -43,6 +43,13 @@ struct NotifyArgs {
 
 size_t notify_workspace_bytes(const Shape& sh);
 
+// Size of the library's static notify scratch (ep_notify_dispatch_noalloc).
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+
+// Device address of that scratch on the current device (looked up once per
+// device, then cached).
+cudaError_t notify_noalloc_scratch(void** out);
+
 // `workspace` must hold notify_workspace_bytes(sh) bytes; the launcher clears
 // it on `stream` first.  stall_block < 0 for normal runs.
 cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace, int stall_block,

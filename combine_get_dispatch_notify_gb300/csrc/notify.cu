@@ -17,8 +17,15 @@
 // small per-rank results (rank prefix matrix, node prefix, per-expert
 // totals, recv_base) from the exchanged counts and cross-checks them with
 // the scan.  Every wait gives up after a deadline and sets EP_DEV_TIMEOUT.
+#include <mutex>
+
 #include "ep_device.cuh"
 #include "ep_internal.h"
+
+// Fixed scratch for ep_notify_dispatch_noalloc, for callers that cannot
+// allocate device memory.  Every GPU that loads the library holds these
+// bytes until the process exits.  All calls share it.
+static __device__ __align__(256) unsigned char g_notify_noalloc_scratch[ep::kNoAllocScratchBytes];
 
 namespace ep {
 namespace {
@@ -276,6 +283,32 @@ __global__ void __launch_bounds__(kNotifyThreads) notify_kernel(NotifyKernelArgs
 }
 
 }  // namespace
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the static scratch on the current device.  The first call
+// on a device looks the address up (with that device current) and caches it.
+// A host-side reference to the array is only a stand-in, never a device
+// address, so kernels must be given this pointer instead.
+cudaError_t notify_noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_notify_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
 
 size_t notify_workspace_bytes(const Shape& sh) {
     const size_t V = static_cast<size_t>(sh.R + sh.N);

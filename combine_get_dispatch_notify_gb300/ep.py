@@ -73,6 +73,7 @@ _SIGS = {
     "ep_notify_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_sz, _vp, _vp, _vp]),
     "ep_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 5 + [_vp]),
     "ep_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i64] + [_vp] * 5 + [_vp]),
+    "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_vp, _vp, _vp]),
     "ep_sync_status": (_i32, [_vp, _vp]),
     "ep_debug_notify_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 +
                                        [_sz, _vp, _i32, _i32, _vp]),
@@ -221,6 +222,25 @@ def ep_notify_dispatch(shape: EpShape, is_token_in_rank, num_tokens_per_rank,
                                   _sz(workspace.numel() * workspace.element_size()),
                                   _t(status, torch.int32, (1,), "status"), host, _stream(stream))
     _check("ep_notify_dispatch", rc)
+
+
+def ep_notify_dispatch_noalloc(shape: EpShape, is_token_in_rank, num_tokens_per_rank,
+                               num_tokens_per_rdma_rank, num_tokens_per_expert, outs: dict, status,
+                               host_num_recv_tokens=None, stream=None) -> None:
+    """ep_notify_dispatch using the library's fixed 1 MiB device scratch instead of a
+    caller workspace, for callers that cannot allocate device memory.  Calls share
+    that scratch, so calls that overlap on the GPU race; ``outs`` needs no
+    "workspace" entry."""
+    args = _notify_args(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                        num_tokens_per_expert, outs)
+    host = _vp(None)
+    if host_num_recv_tokens is not None:
+        if host_num_recv_tokens.dtype != torch.int32 or host_num_recv_tokens.numel() < shape.num_ranks + 1:
+            raise ValueError("host_num_recv_tokens must be int32 with R+1 elements")
+        host = _vp(host_num_recv_tokens.data_ptr())
+    rc = lib().ep_notify_dispatch_noalloc(ctypes.byref(shape), *args,
+                                          _t(status, torch.int32, (1,), "status"), host, _stream(stream))
+    _check("ep_notify_dispatch_noalloc", rc)
 
 
 def ep_debug_notify_dispatch_stall(shape: EpShape, is_token_in_rank, num_tokens_per_rank,

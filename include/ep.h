@@ -195,6 +195,39 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
                                cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * ep_notify_dispatch without a caller-provided workspace.  The paper has no
+ * counterpart; this exists for callers that cannot allocate device memory -
+ * for example code running inside a host framework that owns every device
+ * allocation and hands a plugin only the tensors it must fill, or a serving
+ * loop that forbids allocation after start-up - and so have no way to supply
+ * the workspace.
+ *
+ * Same arguments, outputs and errors as ep_notify_dispatch, minus
+ * `workspace` / `workspace_bytes`.  The scratch is a 1 MiB array compiled
+ * into the library (a static __device__ array); every GPU that loads the
+ * library holds it until the process exits.  A shape whose workspace
+ * (ep_notify_workspace_bytes) exceeds 1 MiB - that is, 256 + R*C*(R+N)*8
+ * bytes - is refused with EP_ERR_INVALID_ARG before anything is enqueued.
+ * The call allocates and frees nothing.
+ *
+ * The first call on each device looks up the array's device address (a
+ * cudaGetSymbolAddress with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array and
+ * each clears it on `stream` before use, so two calls whose executions
+ * overlap on the GPU (different streams without ordering, or concurrent
+ * host threads) race on it and give undefined results; order them.
+ */
+ep_status_t ep_notify_dispatch_noalloc(
+    const ep_shape_t* shape, const uint8_t* is_token_in_rank,
+    const int32_t* num_tokens_per_rank, const int32_t* num_tokens_per_rdma_rank,
+    const int32_t* num_tokens_per_expert, int32_t* rank_prefix_matrix,
+    int32_t* gbl_channel_prefix_matrix, int32_t* rdma_channel_prefix_matrix,
+    int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+    int32_t* recv_channel_offset, int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+    int32_t* num_recv_tokens_per_expert, int64_t* recv_base, int32_t* send_pos, int32_t* status,
+    int32_t* host_num_recv_tokens, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Step 3 - dispatch.  [RT] intranodeDispatch / internodeDispatch (receive
  * side: recv_x, recv_topk_idx, recv_topk_weights, source index), [AR] 4.1
  * (SrcInfo {src_rank, src_idx}).  Token (s,t) is copied to pool row
