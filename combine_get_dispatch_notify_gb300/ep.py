@@ -73,7 +73,7 @@ _SIGS = {
     "ep_notify_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_sz, _vp, _vp, _vp]),
     "ep_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 5 + [_vp]),
     "ep_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i64] + [_vp] * 5 + [_vp]),
-    "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_vp, _vp, _vp]),
+    "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 15 + [_vp, _vp, _vp]),
     "ep_sync_status": (_i32, [_vp, _vp]),
     "ep_debug_notify_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 +
                                        [_sz, _vp, _i32, _i32, _vp]),

@@ -38,6 +38,23 @@ def test_exports_every_declared_symbol(ep):
     assert sorted(ep.exported_symbols()) == names
 
 
+def declared_arity():
+    """Parameter count of every function the header declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(ep_[a-z_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arity_matches_header(ep):
+    arity = declared_arity()
+    lib = ep.lib()
+    for name in ep.exported_symbols():
+        assert len(getattr(lib, name).argtypes) == arity[name], name
+
+
 def test_library_links_against_the_shared_cuda_runtime(ep):
     with open("/proc/self/maps") as f:
         maps = f.read()
