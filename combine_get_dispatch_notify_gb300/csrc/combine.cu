@@ -2,14 +2,17 @@
 // routing).  combined_x[s][t] = bf16_rne(sum over contributing ranks r, in
 // ascending order, of float(y[recv_base[r] + send_pos[s][t][r]])).
 //
-// Work unit = (token, column slice of 32 x 16 bytes).  A warp reads the
-// token's send_pos row (lane r = rank r), compacts the contributing rows in
-// ascending rank order into shared memory, then each lane loads its 16-byte
-// chunk from every contributing row (all loads in flight together),
-// accumulates in fp32 in that order, rounds to bf16 and stores 16 bytes.
-// Slices of one token go to neighbouring warps, so every load of a warp is a
-// contiguous 512-byte segment.  No atomics: the result is deterministic and
-// bit-identical to a sequential fp32 sum in the same order.
+// Work unit = (token, column slice of 32 lanes x 2 chunks x 16 bytes).  A
+// warp reads the token's send_pos row (lane r = rank r), compacts the
+// contributing rows in ascending rank order into shared memory, then each
+// lane loads its two 16-byte chunks from up to 4 contributing rows at a time
+// (8 independent loads in flight per lane), accumulates in fp32 in rank
+// order, rounds to bf16 and stores.  The chunks of a lane are 512 bytes
+// apart, so every load instruction of a warp covers a contiguous 512-byte
+// segment; slices of one token go to neighbouring warps.  Three 256-thread
+// CTAs per SM with the default L1/shared split (the gather uses L1 for the
+// row map).  No atomics: the result is deterministic and bit-identical to a
+// sequential fp32 sum in the same order.
 #include <cuda_bf16.h>
 
 #include "ep_device.cuh"
@@ -21,7 +24,8 @@ namespace {
 constexpr int kCombineThreads = 256;
 constexpr int kCombineWarps = kCombineThreads / kWarp;
 constexpr int kCombineBlocksPerSm = 3;
-constexpr int kBatch = 8;  // contributing rows loaded together
+constexpr int kBatch = 4;  // contributing rows loaded together
+constexpr int kCpl = 2;    // 16-byte chunks per lane per unit
 
 struct CombineArgs {
     const uint8_t* y;
@@ -35,7 +39,7 @@ struct CombineArgs {
     int R, K;
     long long row_bytes;
     int chunks;  // 16-byte chunks per row
-    int slices;  // ceil(chunks / 32)
+    int slices;  // ceil(chunks / (32 * kCpl))
     long long num_units;
 };
 
@@ -63,6 +67,8 @@ combine_kernel(CombineArgs p) {
     __shared__ long long s_base[33];
     __shared__ long long s_rows[kCombineWarps][32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    griddep_launch_dependents();
+    griddep_wait();  // the expert outputs and the row map are visible from here on
     if (tid <= p.R) s_base[tid] = p.recv_base[tid];
     __syncthreads();
     long long* rows = s_rows[warp];
@@ -89,22 +95,31 @@ combine_kernel(CombineArgs p) {
         if (row >= 0) rows[__popc(valid & lanemask_lt())] = row;
         __syncwarp();
 
-        const int ch = slice * kWarp + lane;
-        if (ch < p.chunks) {
-            float acc[8];
+        const int ch0 = slice * kWarp * kCpl + lane;
+        {
+            float acc[kCpl][8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            const long long col = static_cast<long long>(ch) * 16;
+            for (int c = 0; c < kCpl; ++c)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[c][i] = 0.0f;
             for (int j0 = 0; j0 < n; j0 += kBatch) {
-                uint4 v[kBatch];
+                uint4 v[kCpl][kBatch];
 #pragma unroll
                 for (int i = 0; i < kBatch; ++i)
-                    if (j0 + i < n) v[i] = ld_nc_v4(p.y + rows[j0 + i] * p.row_bytes + col);
+#pragma unroll
+                    for (int c = 0; c < kCpl; ++c)
+                        if (j0 + i < n && ch0 + c * kWarp < p.chunks)
+                            v[c][i] = ld_nc_v4(p.y + rows[j0 + i] * p.row_bytes + static_cast<long long>(ch0 + c * kWarp) * 16);
 #pragma unroll
                 for (int i = 0; i < kBatch; ++i)
-                    if (j0 + i < n) add_bf16x8(acc, v[i]);
+#pragma unroll
+                    for (int c = 0; c < kCpl; ++c)
+                        if (j0 + i < n && ch0 + c * kWarp < p.chunks) add_bf16x8(acc[c], v[c][i]);
             }
-            st_v4(p.out + g * p.row_bytes + col, pack_bf16x8(acc));
+#pragma unroll
+            for (int c = 0; c < kCpl; ++c)
+                if (ch0 + c * kWarp < p.chunks)
+                    st_v4(p.out + g * p.row_bytes + static_cast<long long>(ch0 + c * kWarp) * 16, pack_bf16x8(acc[c]));
         }
         if (slice == 0 && p.out_w != nullptr && lane < p.K) {
             float w = 0.0f;
@@ -137,13 +152,13 @@ cudaError_t launch_combine(const Shape& sh, const uint16_t* y, const float* y_w,
     p.K = sh.K;
     p.row_bytes = sh.row_bytes();
     p.chunks = static_cast<int>(p.row_bytes / 16);
-    p.slices = (p.chunks + kWarp - 1) / kWarp;
+    p.slices = (p.chunks + kWarp * kCpl - 1) / (kWarp * kCpl);
     p.num_units = tokens * p.slices;
     const long long want = (p.num_units + kCombineWarps - 1) / kCombineWarps;
     const long long cap = static_cast<long long>(sms) * kCombineBlocksPerSm;
     const long long grid = want < cap ? want : cap;
-    combine_kernel<<<static_cast<unsigned>(grid), kCombineThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), 0,
+                      stream, 0, false, p);
 }
 
 }  // namespace ep

@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     long long* base = reinterpret_cast<long long*>(desc + S);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid <= p.R) base[tid] = p.recv_base[tid];
+    griddep_launch_dependents();
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         }
         fence_mbarrier_init();
     }
+    griddep_wait();  // send_pos / recv_base from notify are visible from here on
+    if (tid <= p.R) base[tid] = p.recv_base[tid];
     __syncthreads();
 
     if (warp == 0) {
@@ -261,12 +263,9 @@ cudaError_t launch_dispatch(const Shape& sh, const uint16_t* x, const int64_t* t
 
     const size_t smem = static_cast<size_t>(slots) * part + 2 * slots * sizeof(uint64_t) +
                         slots * sizeof(SlotDesc) + 33 * sizeof(long long);
-    cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
     const long long grid = p.num_units < grid_target ? p.num_units : grid_target;
-    dispatch_kernel<<<static_cast<unsigned>(grid), kDispatchThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_kernel, dim3(static_cast<unsigned>(grid)), dim3(kDispatchThreads), smem,
+                      stream, 0, true, p);
 }
 
 }  // namespace ep

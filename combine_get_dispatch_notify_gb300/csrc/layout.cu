@@ -62,7 +62,9 @@ layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, 
     int32_t* h_expert = hist;
     int32_t* h_rank = hist + E;
     int32_t* h_node = h_rank + R;
+    griddep_launch_dependents();
     for (int i = tid; i < bins; i += blockDim.x) hist[i] = 0;
+    griddep_wait();  // top-k ids written by the preceding kernel are visible
     __syncthreads();
 
     const int t_begin = min(T, part * tokens_per_cta);
@@ -122,7 +124,10 @@ layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, 
     if (lane < N && node_acc) atomicAdd(&h_node[lane], node_acc);
     if (bad) flag_error(status, EP_DEV_INPUT);
 
-    cluster.sync();  // every CTA's partial histogram is complete and visible
+    if (parts > 1)
+        cluster.sync();  // every CTA's partial histogram is complete and visible
+    else
+        __syncthreads();
     if (part == 0) {
         for (int i = tid; i < bins; i += blockDim.x) {
             int32_t sum = 0;
@@ -135,7 +140,7 @@ layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, 
                 num_tokens_per_rdma_rank[static_cast<int64_t>(s) * N + (i - E - R)] = sum;
         }
     }
-    cluster.sync();  // keep every histogram alive until CTA 0 has read it
+    if (parts > 1) cluster.sync();  // keep every histogram alive until CTA 0 has read it
 }
 
 }  // namespace
@@ -147,27 +152,10 @@ cudaError_t launch_layout(const Shape& sh, const int64_t* topk_idx, int32_t* num
     parts = parts < 1 ? 1 : (parts > kMaxClusterCtas ? kMaxClusterCtas : parts);
     const int tokens_per_cta = (sh.T + parts - 1) / parts;
     const size_t smem = sizeof(int32_t) * static_cast<size_t>(sh.E + sh.R + sh.N);
-    if (smem > 48 * 1024) {
-        cudaError_t e =
-            cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(parts, sh.R, 1);
-    cfg.blockDim = dim3(kLayoutThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = parts;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, layout_kernel, topk_idx, sh.R, sh.T, sh.K, sh.E, sh.N, sh.E_loc,
-                              tokens_per_cta, num_tokens_per_rank, num_tokens_per_rdma_rank,
-                              num_tokens_per_expert, is_token_in_rank, status);
+    return launch_pdl(layout_kernel, dim3(parts, sh.R, 1), dim3(kLayoutThreads, 1, 1), smem, stream,
+                      static_cast<unsigned>(parts), false, topk_idx, sh.R, sh.T, sh.K, sh.E, sh.N, sh.E_loc,
+                      tokens_per_cta, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                      num_tokens_per_expert, is_token_in_rank, status);
 }
 
 }  // namespace ep

@@ -1,22 +1,28 @@
 // Step 2 - notify prefix sums ([IN] notify_dispatch: sm1..x stages 1-3 and
 // sm0 stage 6; [RT] intranode/internodeNotifyDispatch for names and shapes).
 //
-// One CTA per (source rank s, channel c) block, R*C blocks in (s, c) order,
-// which is also the order rows appear in every receive region.  A block
-//   1. counts, per destination rank and per destination node, the tokens of
-//      its channel (warp ballot + popc);
-//   2. publishes that aggregate and looks back over earlier blocks
-//      (single-pass decoupled lookback, one thread per rank / node value) to
-//      get two exclusive prefixes at once: within its source rank (channel
-//      prefix matrices) and global (start row of the block in each
-//      destination region = recv_channel_offset);
-//   3. rewalks its tokens and writes send_pos = block start + running index,
-//      staged through shared memory so the global writes are coalesced.
-// Block order comes from an atomic ticket, so a block only ever waits on
-// blocks that are already running.  The last block to finish computes the
-// small per-rank results (rank prefix matrix, node prefix, per-expert
-// totals, recv_base) from the exchanged counts and cross-checks them with
-// the scan.  Every wait gives up after a deadline and sets EP_DEV_TIMEOUT.
+// Grid = 1 + R*C CTAs, roles taken from an atomic ticket in launch order:
+//   ticket 0      the per-rank results, which depend only on the exchanged
+//                 counts ([IN] sm0 stage 6): rank prefix matrix and its
+//                 transpose, receive counts, node-level prefix, per-expert
+//                 totals rounded up to the alignment, recv_base;
+//   ticket 1+b    block b = (source rank s, channel c), in (s, c) order:
+//     1. count the channel's tokens per destination rank and per node (warp
+//        ballot + popc) - [IN] sm1..x stage 1;
+//     2. publish that aggregate and look back over the earlier channels of
+//        the same source rank (decoupled lookback, one warp per value reading
+//        32 predecessors per probe) for the exclusive within-source prefix
+//        (channel prefix matrices, [IN] stages 2-3);
+//     3. start row of the block in destination r's region = tokens every
+//        earlier source rank sends to r (summed from num_tokens_per_rank, as
+//        the pages' notify derives receive offsets from exchanged counts) +
+//        the within-source prefix; then rewalk the channel and write
+//        send_pos = start + running index, staged through shared memory so
+//        the global writes are coalesced.
+// The last channel of each source checks that its totals equal the count
+// inputs (EP_DEV_INCONSISTENT otherwise).  A block waits only on blocks with
+// smaller tickets, which are already running; every wait gives up after a
+// deadline and sets EP_DEV_TIMEOUT.
 #include <mutex>
 
 #include "ep_device.cuh"
@@ -32,29 +38,24 @@ namespace {
 
 constexpr int kNotifyThreads = 256;
 constexpr int kNotifyWarps = kNotifyThreads / kWarp;
-constexpr int kWorkspaceHeader = 256;  // two counters, padded
+constexpr int kWorkspaceHeader = 256;  // ticket counter, padded
 
-// Lookback word: [63:62] flag, [61:31] within-source prefix, [30:0] global prefix.
+// Lookback word: [63:62] flag (0 = not yet published), [30:0] value.
 constexpr unsigned long long kFlagAggregate = 1ull;
 constexpr unsigned long long kFlagPrefix = 2ull;
 constexpr unsigned long long kMask31 = (1ull << 31) - 1;
 
-__device__ __forceinline__ unsigned long long pack_word(unsigned long long flag, uint32_t seg,
-                                                        uint32_t glob) {
-    return (flag << 62) | ((static_cast<unsigned long long>(seg) & kMask31) << 31) |
-           (static_cast<unsigned long long>(glob) & kMask31);
+__device__ __forceinline__ unsigned long long pack_word(unsigned long long flag, uint32_t val) {
+    return (flag << 62) | (static_cast<unsigned long long>(val) & kMask31);
 }
-__device__ __forceinline__ uint32_t word_seg(unsigned long long w) {
-    return static_cast<uint32_t>((w >> 31) & kMask31);
-}
-__device__ __forceinline__ uint32_t word_glob(unsigned long long w) {
+__device__ __forceinline__ uint32_t word_val(unsigned long long w) {
     return static_cast<uint32_t>(w & kMask31);
 }
 
 struct NotifyKernelArgs {
     NotifyArgs a;
-    unsigned* counters;        // [0] ticket, [1] finished blocks
-    unsigned long long* words; // [R*C][V]
+    unsigned* counters;        // [0] ticket
+    unsigned long long* words; // [R*C][V], V = R + N values per block
     int R, T, E, C, N, E_loc, align, q, V;
     int stall_block;
     long long wait_limit_ns;
@@ -92,51 +93,41 @@ __device__ __forceinline__ uint32_t node_bits(uint32_t m, int R, int N) {
     return nm;
 }
 
-__device__ void finish(const NotifyKernelArgs& p, int32_t* s_nrecv) {
+// Ticket 0: the per-rank results ([IN] sm0 stage 6), from the count inputs only.
+__device__ void per_rank_results(const NotifyKernelArgs& p, int32_t* s_nrecv) {
     const NotifyArgs& a = p.a;
-    const int R = p.R, N = p.N, C = p.C, V = p.V, tid = threadIdx.x;
-    bool inconsistent = false;
-    // [IN] sm0 stage 6: prefix of per-rank counts over global source rank.
+    const int R = p.R, N = p.N, tid = threadIdx.x;
+    // prefix of per-rank counts over global source rank
     for (int r = tid; r < R; r += blockDim.x) {
         int32_t run = 0;
         for (int s = 0; s < R; ++s) {
-            run += a.num_tokens_per_rank[static_cast<int64_t>(s) * R + r];
+            run += __ldg(a.num_tokens_per_rank + static_cast<int64_t>(s) * R + r);
             a.rank_prefix_matrix[static_cast<int64_t>(s) * R + r] = run;
             a.recv_gbl_rank_prefix_sum[static_cast<int64_t>(r) * R + s] = run;
-            const unsigned long long w =
-                ld_acquire_u64(p.words + (static_cast<int64_t>(s) * C + C - 1) * V + r);
-            if (word_glob(w) != static_cast<uint32_t>(run)) inconsistent = true;
         }
         a.num_recv_tokens[r] = run;
         s_nrecv[r] = run;
     }
-    // Node-level receive prefix: rank r receives for its node from the
-    // same-GPU-index peer m*8 + r%8 of every node m.
+    // node-level receive prefix: rank r receives for its node from the
+    // same-GPU-index peer m*8 + r%8 of every node m
     for (int r = tid; r < R; r += blockDim.x) {
         int32_t run = 0;
         for (int m = 0; m < N; ++m) {
             const int peer = m * kNodeSize + r % kNodeSize;
-            run += a.num_tokens_per_rdma_rank[static_cast<int64_t>(peer) * N + r / kNodeSize];
+            run += __ldg(a.num_tokens_per_rdma_rank + static_cast<int64_t>(peer) * N + r / kNodeSize);
             a.recv_rdma_rank_prefix_sum[static_cast<int64_t>(r) * N + m] = run;
         }
         a.num_rdma_recv_tokens[r] = run;
     }
-    for (int i = tid; i < R * N; i += blockDim.x) {
-        const int s = i / N, n = i % N;
-        const unsigned long long w =
-            ld_acquire_u64(p.words + (static_cast<int64_t>(s) * C + C - 1) * V + R + n);
-        if (word_seg(w) != static_cast<uint32_t>(a.num_tokens_per_rdma_rank[i])) inconsistent = true;
-    }
-    // Per-expert receive counts, rounded up to the alignment.
+    // per-expert receive counts, rounded up to the alignment
     for (int i = tid; i < R * p.E_loc; i += blockDim.x) {
         const int r = i / p.E_loc, j = i % p.E_loc;
         long long sum = 0;
         for (int s = 0; s < R; ++s)
-            sum += a.num_tokens_per_expert[static_cast<int64_t>(s) * p.E + r * p.E_loc + j];
+            sum += __ldg(a.num_tokens_per_expert + static_cast<int64_t>(s) * p.E + r * p.E_loc + j);
         sum = (sum + p.align - 1) / p.align * p.align;
         a.num_recv_tokens_per_expert[i] = static_cast<int32_t>(sum);
     }
-    if (inconsistent) flag_error(a.status, EP_DEV_INCONSISTENT);
     __syncthreads();
     if (tid == 0) {
         long long acc = 0;
@@ -153,25 +144,72 @@ __device__ void finish(const NotifyKernelArgs& p, int32_t* s_nrecv) {
     }
 }
 
+// Exclusive prefix of value v over blocks [seg_lo, b) (one warp).  Lanes read
+// 32 predecessors at once; the nearest published inclusive prefix ends the
+// walk, and the segment start acts as one with value 0.
+__device__ uint32_t segment_lookback(const NotifyKernelArgs& p, int b, int seg_lo, int v,
+                                     int lane, long long deadline, bool& timed_out) {
+    uint32_t excl = 0;
+    for (int j0 = b - 1; j0 >= seg_lo; j0 -= kWarp) {
+        const int j = j0 - lane;
+        unsigned long long word = pack_word(kFlagPrefix, 0);
+        if (j >= seg_lo) {
+            const unsigned long long* w = p.words + static_cast<int64_t>(j) * p.V + v;
+            word = ld_acquire_u64(w);
+            uint32_t polls = 0;
+            while ((word >> 62) == 0ull) {
+                if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
+                    timed_out = true;
+                    word = pack_word(kFlagPrefix, 0);
+                    break;
+                }
+                __nanosleep(32);
+                word = ld_acquire_u64(w);
+            }
+        }
+        const unsigned pm = __ballot_sync(0xffffffffu, (word >> 62) == kFlagPrefix);
+        const uint32_t val = word_val(word);
+        if (pm != 0u) {
+            const int k = __ffs(pm) - 1;
+            excl += __reduce_add_sync(0xffffffffu, lane <= k ? val : 0u);
+            break;
+        }
+        excl += __reduce_add_sync(0xffffffffu, val);
+    }
+    return excl;
+}
+
 __global__ void __launch_bounds__(kNotifyThreads) notify_kernel(NotifyKernelArgs p) {
     extern __shared__ int32_t tile[];  // [kNotifyThreads][R + 1] send_pos staging
-    __shared__ int s_block, s_last;
+    __shared__ int s_ticket;
     __shared__ int32_t s_count[64];    // block totals: ranks, then nodes
-    __shared__ int32_t s_start[32];    // global start row of this block, per rank
+    __shared__ int32_t s_segex[64];    // exclusive within-source prefix per value
+    __shared__ int32_t s_start[32];    // start row of this block in each region
     __shared__ int32_t s_run[32];      // running count inside the channel
     __shared__ int32_t s_warp[kNotifyWarps][33];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int R = p.R, N = p.N, C = p.C, V = p.V, T = p.T;
-    if (tid == 0) s_block = static_cast<int>(atomicAdd(p.counters, 1u));
+    griddep_launch_dependents();
+    griddep_wait();  // the layout outputs are complete from here on
+    if (tid == 0) s_ticket = static_cast<int>(atomicAdd(p.counters, 1u));
     if (tid < 64) s_count[tid] = 0;
     if (tid < 32) s_run[tid] = 0;
     __syncthreads();
-    const int b = s_block, s = b / C, c = b % C;
+    if (s_ticket == 0) {
+        per_rank_results(p, s_run);
+        return;
+    }
+    const int b = s_ticket - 1, s = b / C, c = b % C;
     const int t0 = min(c * p.q, T), t1 = min(t0 + p.q, T);
     const uint8_t* in_rank = p.a.is_token_in_rank + static_cast<int64_t>(s) * T * R;
 
-    // 1. per-rank / per-node counts of the channel ([IN] sm1..x stage 1)
+    // tokens every earlier source rank sends to r (independent loads, issued early)
+    int32_t cross = 0;
+    if (tid < R)
+        for (int s2 = 0; s2 < s; ++s2) cross += __ldg(p.a.num_tokens_per_rank + static_cast<int64_t>(s2) * R + tid);
+
+    // 1. per-rank / per-node counts of the channel
     int rank_acc = 0, node_acc = 0;
     for (int base = t0; base < t1; base += kNotifyThreads) {
         const int t = base + tid;
@@ -190,54 +228,47 @@ __global__ void __launch_bounds__(kNotifyThreads) notify_kernel(NotifyKernelArgs
     if (lane < N && node_acc) atomicAdd(&s_count[R + lane], node_acc);
     __syncthreads();
 
-    // 2. publish, look back, publish the inclusive prefix ([IN] stages 2-3)
-    if (tid < V) {
-        const int v = tid;
-        const uint32_t agg = static_cast<uint32_t>(s_count[v]);
-        unsigned long long* mine = p.words + static_cast<int64_t>(b) * V + v;
-        uint32_t ex_seg = 0, ex_glob = 0;
-        if (b != p.stall_block) {
-            if (b == 0) {
-                st_release_u64(mine, pack_word(kFlagPrefix, agg, agg));
-            } else {
-                st_release_u64(mine, pack_word(kFlagAggregate, agg, agg));
-                const long long deadline = globaltimer_ns() + p.wait_limit_ns;
-                bool timed_out = false;
-                for (int j = b - 1; j >= 0 && !timed_out; --j) {
-                    const unsigned long long* w = p.words + static_cast<int64_t>(j) * V + v;
-                    unsigned long long word = ld_acquire_u64(w);
-                    uint32_t polls = 0;
-                    while ((word >> 62) == 0ull) {
-                        if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
-                            timed_out = true;
-                            break;
-                        }
-                        __nanosleep(64);
-                        word = ld_acquire_u64(w);
-                    }
-                    if (timed_out) break;
-                    ex_glob += word_glob(word);
-                    if (j / C == s) ex_seg += word_seg(word);
-                    if ((word >> 62) == kFlagPrefix) break;
-                }
-                if (timed_out) flag_error(p.a.status, EP_DEV_TIMEOUT);
-                st_release_u64(mine, pack_word(kFlagPrefix, ex_seg + agg, ex_glob + agg));
-            }
-            if (v < R) {
-                p.a.gbl_channel_prefix_matrix[(static_cast<int64_t>(s) * R + v) * C + c] =
-                    static_cast<int32_t>(ex_seg + agg);
-                p.a.recv_channel_offset[(static_cast<int64_t>(v) * R + s) * C + c] =
-                    static_cast<int32_t>(ex_glob);
-            } else {
-                p.a.rdma_channel_prefix_matrix[(static_cast<int64_t>(s) * N + (v - R)) * C + c] =
-                    static_cast<int32_t>(ex_seg + agg);
-            }
+    // 2. publish the aggregate (the first channel of a source publishes its
+    //    inclusive prefix directly), then look back within the source rank
+    unsigned long long* mine = p.words + static_cast<int64_t>(b) * V;
+    if (tid < V && b != p.stall_block)
+        st_release_u64(mine + tid, pack_word(c == 0 ? kFlagPrefix : kFlagAggregate,
+                                             static_cast<uint32_t>(s_count[tid])));
+    __syncthreads();
+    bool timed_out = false;
+    const long long deadline = globaltimer_ns() + p.wait_limit_ns;
+    for (int v = warp; v < V; v += kNotifyWarps) {
+        const uint32_t ex = c == 0 ? 0u : segment_lookback(p, b, s * C, v, lane, deadline, timed_out);
+        if (lane == 0) {
+            s_segex[v] = static_cast<int32_t>(ex);
+            if (c != 0 && b != p.stall_block)
+                st_release_u64(mine + v, pack_word(kFlagPrefix, ex + static_cast<uint32_t>(s_count[v])));
         }
-        if (v < R) s_start[v] = static_cast<int32_t>(ex_glob);
+    }
+    if (__any_sync(0xffffffffu, timed_out) && lane == 0) flag_error(p.a.status, EP_DEV_TIMEOUT);
+    __syncthreads();
+
+    // 3. outputs of the block; the last channel checks the totals
+    if (tid < V) {
+        const int32_t incl = s_segex[tid] + s_count[tid];
+        bool bad = false;
+        if (tid < R) {
+            const int r = tid;
+            p.a.gbl_channel_prefix_matrix[(static_cast<int64_t>(s) * R + r) * C + c] = incl;
+            p.a.recv_channel_offset[(static_cast<int64_t>(r) * R + s) * C + c] = cross + s_segex[r];
+            s_start[r] = cross + s_segex[r];
+            if (c == C - 1) bad = incl != __ldg(p.a.num_tokens_per_rank + static_cast<int64_t>(s) * R + r);
+        } else {
+            const int n = tid - R;
+            p.a.rdma_channel_prefix_matrix[(static_cast<int64_t>(s) * N + n) * C + c] = incl;
+            if (c == C - 1)
+                bad = incl != __ldg(p.a.num_tokens_per_rdma_rank + static_cast<int64_t>(s) * N + n);
+        }
+        if (bad) flag_error(p.a.status, EP_DEV_INCONSISTENT);
     }
     __syncthreads();
 
-    // 3. send_pos = block start + running index of the token among the
+    // 4. send_pos = start row + running index of the token among the
     //    channel's tokens routed to the same rank
     int32_t* send_pos = p.a.send_pos + static_cast<int64_t>(s) * T * R;
     const int stride = R + 1;
@@ -271,15 +302,6 @@ __global__ void __launch_bounds__(kNotifyThreads) notify_kernel(NotifyKernelArgs
         for (int i = tid; i < n_int; i += kNotifyThreads) dst[i] = tile[(i / R) * stride + (i % R)];
         __syncthreads();
     }
-
-    // last block to finish computes the per-rank results
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(p.counters + 1, 1u) == gridDim.x - 1u;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    finish(p, s_run);  // s_run is free now: reuse it for the per-rank totals
 }
 
 }  // namespace
@@ -336,9 +358,8 @@ cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace,
     p.stall_block = stall_block;
     p.wait_limit_ns = wait_limit_ns;
     const size_t smem = sizeof(int32_t) * kNotifyThreads * static_cast<size_t>(sh.R + 1);
-    const int blocks = sh.R * sh.C;
-    notify_kernel<<<blocks, kNotifyThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    const unsigned blocks = 1u + static_cast<unsigned>(sh.R * sh.C);
+    return launch_pdl(notify_kernel, dim3(blocks), dim3(kNotifyThreads), smem, stream, 0, false, p);
 }
 
 }  // namespace ep

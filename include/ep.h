@@ -135,8 +135,10 @@ ep_status_t ep_get_dispatch_layout(const ep_shape_t* shape, const int64_t* topk_
  * prefix) and sm0 stage 6 (per-rank prefix over global source rank, node
  * prefix, per-expert totals rounded up to expert_alignment); [RT]
  * intranodeNotifyDispatch / internodeNotifyDispatch for the outputs' names
- * and shapes.  One single-pass decoupled-lookback scan over the R*C
- * (source rank, channel) blocks.
+ * and shapes.  One kernel: per (source rank, channel) block a count, then a
+ * decoupled-lookback scan over the channels of the same source rank; the
+ * offset contributed by earlier source ranks comes from the per-rank counts,
+ * as in the pages' notify.
  *
  * Inputs (as produced by step 1):
  *   is_token_in_rank           uint8 [R][T][R]
@@ -176,9 +178,9 @@ ep_status_t ep_get_dispatch_layout(const ep_shape_t* shape, const int64_t* topk_
  *                              stream sync without another copy
  * Rows of r's region are ordered by (source rank, channel, token), which is
  * (source rank, token) order.  If the count inputs disagree with
- * is_token_in_rank, EP_DEV_INCONSISTENT is set (the outputs then follow
- * is_token_in_rank for the channel matrices and send_pos, and the count
- * inputs for the rest).  A bounded wait that runs out sets EP_DEV_TIMEOUT.
+ * is_token_in_rank, EP_DEV_INCONSISTENT is set and the outputs are
+ * unspecified (dispatch and combine still never touch memory outside their
+ * buffers).  A bounded wait that runs out sets EP_DEV_TIMEOUT.
  */
 ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_in_rank,
                                const int32_t* num_tokens_per_rank,
