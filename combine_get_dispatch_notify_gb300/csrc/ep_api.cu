@@ -64,7 +64,8 @@ ep_status_t notify_common(const ep_shape_t* shape, const uint8_t* is_token_in_ra
                           int32_t* num_rdma_recv_tokens, int32_t* num_recv_tokens_per_expert,
                           int64_t* recv_base, int32_t* send_pos, void* workspace,
                           size_t workspace_bytes, int32_t* status, int32_t* host_num_recv_tokens,
-                          int stall_block, long long wait_limit_ns, cudaStream_t stream) {
+                          bool clear_workspace, bool force_lookback, int stall_block,
+                          long long wait_limit_ns, cudaStream_t stream) {
     Shape sh;
     if (!make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
     const long long tok_rank = static_cast<long long>(sh.R) * sh.T * sh.R;
@@ -97,7 +98,9 @@ ep_status_t notify_common(const ep_shape_t* shape, const uint8_t* is_token_in_ra
     a.send_pos = send_pos;
     a.status = status;
     a.host_num_recv_tokens = host_num_recv_tokens;
-    return from_cuda(launch_notify(sh, a, workspace, stall_block, wait_limit_ns, stream));
+    return from_cuda(
+        launch_notify(sh, a, workspace, clear_workspace, force_lookback, stall_block, wait_limit_ns,
+                      stream));
 }
 
 }  // namespace
@@ -166,7 +169,7 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
                              rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
                              recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
                              num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos,
-                             workspace, workspace_bytes, status, host_num_recv_tokens, -1,
+                             workspace, workspace_bytes, status, host_num_recv_tokens, false, false, -1,
                              ep::kDefaultWaitLimitNs, stream);
 }
 
@@ -190,7 +193,7 @@ ep_status_t ep_notify_dispatch_noalloc(
                              rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
                              recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
                              num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos,
-                             scratch, ep::kNoAllocScratchBytes, status, host_num_recv_tokens, -1,
+                             scratch, ep::kNoAllocScratchBytes, status, host_num_recv_tokens, true, false, -1,
                              ep::kDefaultWaitLimitNs, stream);
 }
 
@@ -209,7 +212,7 @@ ep_status_t ep_debug_notify_dispatch_stall(
                              rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
                              recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
                              num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos,
-                             workspace, workspace_bytes, status, nullptr, stall_block,
+                             workspace, workspace_bytes, status, nullptr, false, true, stall_block,
                              static_cast<long long>(wait_limit_us) * 1000LL, stream);
 }
 

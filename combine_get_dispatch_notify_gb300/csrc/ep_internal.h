@@ -50,10 +50,14 @@ constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 // device, then cached).
 cudaError_t notify_noalloc_scratch(void** out);
 
-// `workspace` must hold notify_workspace_bytes(sh) bytes; the launcher clears
-// it on `stream` first.  stall_block < 0 for normal runs.
-cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace, int stall_block,
-                          long long wait_limit_ns, cudaStream_t stream);
+// `workspace` must hold notify_workspace_bytes(sh) bytes and be zero before
+// its first use; calls keep it valid for the next call.  With
+// clear_workspace the launcher zeroes it on `stream` first.  force_lookback
+// keeps the inter-block lookback scan even for small sources (test hooks).
+// stall_block < 0 for normal runs.
+cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace, bool clear_workspace,
+                          bool force_lookback, int stall_block, long long wait_limit_ns,
+                          cudaStream_t stream);
 
 cudaError_t launch_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
                             const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,

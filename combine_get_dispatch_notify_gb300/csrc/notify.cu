@@ -9,10 +9,12 @@
 //   ticket 1+b    block b = (source rank s, channel c), in (s, c) order:
 //     1. count the channel's tokens per destination rank and per node (warp
 //        ballot + popc) - [IN] sm1..x stage 1;
-//     2. publish that aggregate and look back over the earlier channels of
-//        the same source rank (decoupled lookback, one warp per value reading
-//        32 predecessors per probe) for the exclusive within-source prefix
-//        (channel prefix matrices, [IN] stages 2-3);
+//     2. get the exclusive within-source prefix (channel prefix matrices,
+//        [IN] stages 2-3): for small sources by recounting the earlier
+//        channels of the source directly (no block waits on another, roles
+//        come from blockIdx); otherwise publish the aggregate and look back
+//        over the earlier channels of the same source (decoupled lookback,
+//        one warp per value reading 32 predecessors per probe);
 //     3. start row of the block in destination r's region = tokens every
 //        earlier source rank sends to r (summed from num_tokens_per_rank, as
 //        the pages' notify derives receive offsets from exchanged counts) +
@@ -38,25 +40,37 @@ namespace {
 
 constexpr int kNotifyThreads = 256;
 constexpr int kNotifyWarps = kNotifyThreads / kWarp;
-constexpr int kWorkspaceHeader = 256;  // ticket counter, padded
+constexpr int kWorkspaceHeader = 256;  // ticket word, padded
 
-// Lookback word: [63:62] flag (0 = not yet published), [30:0] value.
-constexpr unsigned long long kFlagAggregate = 1ull;
-constexpr unsigned long long kFlagPrefix = 2ull;
-constexpr unsigned long long kMask31 = (1ull << 31) - 1;
+// Workspace state survives between calls, so no call has to clear it (only
+// a fresh workspace must be zero).  The 64-bit ticket word holds [63:32] the
+// sequence number of the last completed call and [31:0] the tickets taken by
+// the running call; the block that takes the last ticket stores the next
+// sequence number with a zero count.  Lookback words carry the sequence
+// number of the call that wrote them, so words left by earlier calls read as
+// "not yet published":  [63:32] sequence, [31:30] flag, [29:0] value.
+constexpr unsigned kFlagAggregate = 1u;
+constexpr unsigned kFlagPrefix = 2u;
+constexpr unsigned long long kValMask = (1ull << 30) - 1;
 
-__device__ __forceinline__ unsigned long long pack_word(unsigned long long flag, uint32_t val) {
-    return (flag << 62) | (static_cast<unsigned long long>(val) & kMask31);
+__device__ __forceinline__ unsigned long long pack_word(unsigned seq, unsigned flag, uint32_t val) {
+    return (static_cast<unsigned long long>(seq) << 32) | (static_cast<unsigned long long>(flag) << 30) |
+           (static_cast<unsigned long long>(val) & kValMask);
+}
+__device__ __forceinline__ unsigned word_seq(unsigned long long w) { return static_cast<unsigned>(w >> 32); }
+__device__ __forceinline__ unsigned word_flag(unsigned long long w) {
+    return static_cast<unsigned>((w >> 30) & 3u);
 }
 __device__ __forceinline__ uint32_t word_val(unsigned long long w) {
-    return static_cast<uint32_t>(w & kMask31);
+    return static_cast<uint32_t>(w & kValMask);
 }
 
 struct NotifyKernelArgs {
     NotifyArgs a;
-    unsigned* counters;        // [0] ticket
+    unsigned long long* ticket; // see the workspace state note above
     unsigned long long* words; // [R*C][V], V = R + N values per block
     int R, T, E, C, N, E_loc, align, q, V;
+    int recount;  // 1: recount earlier channels of the source instead of looking back
     int stall_block;
     long long wait_limit_ns;
 };
@@ -93,20 +107,20 @@ __device__ __forceinline__ uint32_t node_bits(uint32_t m, int R, int N) {
     return nm;
 }
 
-// Ticket 0: the per-rank results ([IN] sm0 stage 6), from the count inputs only.
-__device__ void per_rank_results(const NotifyKernelArgs& p, int32_t* s_nrecv) {
+// Ticket 0: the per-rank results ([IN] sm0 stage 6), from the count inputs
+// only.  All inputs are loaded up front by many threads, then summed.
+__device__ void per_rank_results(const NotifyKernelArgs& p, int32_t* s_nrecv,
+                                 int32_t (*s_ntpr)[33]) {
     const NotifyArgs& a = p.a;
     const int R = p.R, N = p.N, tid = threadIdx.x;
-    // prefix of per-rank counts over global source rank
-    for (int r = tid; r < R; r += blockDim.x) {
-        int32_t run = 0;
-        for (int s = 0; s < R; ++s) {
-            run += __ldg(a.num_tokens_per_rank + static_cast<int64_t>(s) * R + r);
-            a.rank_prefix_matrix[static_cast<int64_t>(s) * R + r] = run;
-            a.recv_gbl_rank_prefix_sum[static_cast<int64_t>(r) * R + s] = run;
-        }
-        a.num_recv_tokens[r] = run;
-        s_nrecv[r] = run;
+    for (int i = tid; i < R * R; i += blockDim.x) s_ntpr[i / R][i % R] = __ldg(a.num_tokens_per_rank + i);
+    // per-expert receive counts (expert e = r * E_loc + j), rounded up to the alignment
+    for (int e = tid; e < p.E; e += blockDim.x) {
+        long long sum = 0;
+#pragma unroll 8
+        for (int s = 0; s < R; ++s) sum += __ldg(a.num_tokens_per_expert + static_cast<int64_t>(s) * p.E + e);
+        sum = (sum + p.align - 1) / p.align * p.align;
+        a.num_recv_tokens_per_expert[e] = static_cast<int32_t>(sum);
     }
     // node-level receive prefix: rank r receives for its node from the
     // same-GPU-index peer m*8 + r%8 of every node m
@@ -119,14 +133,17 @@ __device__ void per_rank_results(const NotifyKernelArgs& p, int32_t* s_nrecv) {
         }
         a.num_rdma_recv_tokens[r] = run;
     }
-    // per-expert receive counts, rounded up to the alignment
-    for (int i = tid; i < R * p.E_loc; i += blockDim.x) {
-        const int r = i / p.E_loc, j = i % p.E_loc;
-        long long sum = 0;
-        for (int s = 0; s < R; ++s)
-            sum += __ldg(a.num_tokens_per_expert + static_cast<int64_t>(s) * p.E + r * p.E_loc + j);
-        sum = (sum + p.align - 1) / p.align * p.align;
-        a.num_recv_tokens_per_expert[i] = static_cast<int32_t>(sum);
+    __syncthreads();
+    // prefix of per-rank counts over global source rank
+    for (int r = tid; r < R; r += blockDim.x) {
+        int32_t run = 0;
+        for (int s = 0; s < R; ++s) {
+            run += s_ntpr[s][r];
+            a.rank_prefix_matrix[static_cast<int64_t>(s) * R + r] = run;
+            a.recv_gbl_rank_prefix_sum[static_cast<int64_t>(r) * R + s] = run;
+        }
+        a.num_recv_tokens[r] = run;
+        s_nrecv[r] = run;
     }
     __syncthreads();
     if (tid == 0) {
@@ -147,27 +164,27 @@ __device__ void per_rank_results(const NotifyKernelArgs& p, int32_t* s_nrecv) {
 // Exclusive prefix of value v over blocks [seg_lo, b) (one warp).  Lanes read
 // 32 predecessors at once; the nearest published inclusive prefix ends the
 // walk, and the segment start acts as one with value 0.
-__device__ uint32_t segment_lookback(const NotifyKernelArgs& p, int b, int seg_lo, int v,
+__device__ uint32_t segment_lookback(const NotifyKernelArgs& p, unsigned seq, int b, int seg_lo, int v,
                                      int lane, long long deadline, bool& timed_out) {
     uint32_t excl = 0;
     for (int j0 = b - 1; j0 >= seg_lo; j0 -= kWarp) {
         const int j = j0 - lane;
-        unsigned long long word = pack_word(kFlagPrefix, 0);
+        unsigned long long word = pack_word(seq, kFlagPrefix, 0);
         if (j >= seg_lo) {
             const unsigned long long* w = p.words + static_cast<int64_t>(j) * p.V + v;
             word = ld_acquire_u64(w);
             uint32_t polls = 0;
-            while ((word >> 62) == 0ull) {
+            while (word_seq(word) != seq) {  // not yet published by this call
                 if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
                     timed_out = true;
-                    word = pack_word(kFlagPrefix, 0);
+                    word = pack_word(seq, kFlagPrefix, 0);
                     break;
                 }
                 __nanosleep(32);
                 word = ld_acquire_u64(w);
             }
         }
-        const unsigned pm = __ballot_sync(0xffffffffu, (word >> 62) == kFlagPrefix);
+        const unsigned pm = __ballot_sync(0xffffffffu, word_flag(word) == kFlagPrefix);
         const uint32_t val = word_val(word);
         if (pm != 0u) {
             const int k = __ffs(pm) - 1;
@@ -182,6 +199,8 @@ __device__ uint32_t segment_lookback(const NotifyKernelArgs& p, int b, int seg_l
 __global__ void __launch_bounds__(kNotifyThreads) notify_kernel(NotifyKernelArgs p) {
     extern __shared__ int32_t tile[];  // [kNotifyThreads][R + 1] send_pos staging
     __shared__ int s_ticket;
+    __shared__ unsigned s_seq;
+    __shared__ int32_t s_ntpr[32][33];
     __shared__ int32_t s_count[64];    // block totals: ranks, then nodes
     __shared__ int32_t s_segex[64];    // exclusive within-source prefix per value
     __shared__ int32_t s_start[32];    // start row of this block in each region
@@ -192,12 +211,31 @@ __global__ void __launch_bounds__(kNotifyThreads) notify_kernel(NotifyKernelArgs
     const int R = p.R, N = p.N, C = p.C, V = p.V, T = p.T;
     griddep_launch_dependents();
     griddep_wait();  // the layout outputs are complete from here on
-    if (tid == 0) s_ticket = static_cast<int>(atomicAdd(p.counters, 1u));
-    if (tid < 64) s_count[tid] = 0;
+    if (p.recount) {  // no block waits on another: roles straight from blockIdx
+        if (tid == 0) {
+            s_ticket = static_cast<int>(blockIdx.x);
+            s_seq = 0u;
+        }
+    } else if (tid == 0) {
+        const unsigned long long old = atomicAdd(p.ticket, 1ull);
+        const unsigned taken = static_cast<unsigned>(old & 0xffffffffull);
+        const unsigned seq = static_cast<unsigned>(old >> 32) + 1u;
+        if (taken == gridDim.x - 1u)  // last ticket of this call: arm the next call
+            atomicExch(p.ticket, static_cast<unsigned long long>(seq) << 32);
+        if (taken >= gridDim.x) flag_error(p.a.status, EP_DEV_INCONSISTENT);  // workspace not zeroed
+        s_ticket = taken < gridDim.x ? static_cast<int>(taken) : -1;
+        s_seq = seq;
+    }
+    if (tid < 64) {
+        s_count[tid] = 0;
+        s_segex[tid] = 0;
+    }
     if (tid < 32) s_run[tid] = 0;
     __syncthreads();
+    if (s_ticket < 0) return;
+    const unsigned seq = s_seq;
     if (s_ticket == 0) {
-        per_rank_results(p, s_run);
+        per_rank_results(p, s_run, s_ntpr);
         return;
     }
     const int b = s_ticket - 1, s = b / C, c = b % C;
@@ -206,47 +244,87 @@ __global__ void __launch_bounds__(kNotifyThreads) notify_kernel(NotifyKernelArgs
 
     // tokens every earlier source rank sends to r (independent loads, issued early)
     int32_t cross = 0;
-    if (tid < R)
+    if (tid < R) {
+#pragma unroll 8
         for (int s2 = 0; s2 < s; ++s2) cross += __ldg(p.a.num_tokens_per_rank + static_cast<int64_t>(s2) * R + tid);
-
-    // 1. per-rank / per-node counts of the channel
-    int rank_acc = 0, node_acc = 0;
-    for (int base = t0; base < t1; base += kNotifyThreads) {
-        const int t = base + tid;
-        const uint32_t m = t < t1 ? load_mask(in_rank + static_cast<int64_t>(t) * R, R) : 0u;
-        const uint32_t nm = node_bits(m, R, N);
-        for (int r = 0; r < R; ++r) {
-            const unsigned bb = __ballot_sync(0xffffffffu, (m >> r) & 1u);
-            if (lane == r) rank_acc += __popc(bb);
-        }
-        for (int n = 0; n < N; ++n) {
-            const unsigned bb = __ballot_sync(0xffffffffu, (nm >> n) & 1u);
-            if (lane == n) node_acc += __popc(bb);
-        }
     }
-    if (lane < R && rank_acc) atomicAdd(&s_count[lane], rank_acc);
-    if (lane < N && node_acc) atomicAdd(&s_count[R + lane], node_acc);
-    __syncthreads();
 
-    // 2. publish the aggregate (the first channel of a source publishes its
-    //    inclusive prefix directly), then look back within the source rank
-    unsigned long long* mine = p.words + static_cast<int64_t>(b) * V;
-    if (tid < V && b != p.stall_block)
-        st_release_u64(mine + tid, pack_word(c == 0 ? kFlagPrefix : kFlagAggregate,
-                                             static_cast<uint32_t>(s_count[tid])));
-    __syncthreads();
-    bool timed_out = false;
-    const long long deadline = globaltimer_ns() + p.wait_limit_ns;
-    for (int v = warp; v < V; v += kNotifyWarps) {
-        const uint32_t ex = c == 0 ? 0u : segment_lookback(p, b, s * C, v, lane, deadline, timed_out);
-        if (lane == 0) {
-            s_segex[v] = static_cast<int32_t>(ex);
-            if (c != 0 && b != p.stall_block)
-                st_release_u64(mine + v, pack_word(kFlagPrefix, ex + static_cast<uint32_t>(s_count[v])));
+    if (p.recount) {
+        // 1'+2'. small sources: count the channel (-> s_count) and, directly,
+        //        every earlier channel of the same source (-> s_segex)
+        int pre_r = 0, agg_r = 0, pre_n = 0, agg_n = 0;
+        for (int base = 0; base < t1; base += kNotifyThreads) {
+            const int t = base + tid;
+            const uint32_t m = t < t1 ? load_mask(in_rank + static_cast<int64_t>(t) * R, R) : 0u;
+            const uint32_t mp = t < t0 ? m : 0u, ma = t < t0 ? 0u : m;
+            const uint32_t nmp = node_bits(mp, R, N), nma = node_bits(ma, R, N);
+            for (int r = 0; r < R; ++r) {
+                const unsigned bp = __ballot_sync(0xffffffffu, (mp >> r) & 1u);
+                const unsigned ba = __ballot_sync(0xffffffffu, (ma >> r) & 1u);
+                if (lane == r) {
+                    pre_r += __popc(bp);
+                    agg_r += __popc(ba);
+                }
+            }
+            for (int n = 0; n < N; ++n) {
+                const unsigned bp = __ballot_sync(0xffffffffu, (nmp >> n) & 1u);
+                const unsigned ba = __ballot_sync(0xffffffffu, (nma >> n) & 1u);
+                if (lane == n) {
+                    pre_n += __popc(bp);
+                    agg_n += __popc(ba);
+                }
+            }
         }
+        if (lane < R && (pre_r | agg_r)) {
+            atomicAdd(&s_segex[lane], pre_r);
+            atomicAdd(&s_count[lane], agg_r);
+        }
+        if (lane < N && (pre_n | agg_n)) {
+            atomicAdd(&s_segex[R + lane], pre_n);
+            atomicAdd(&s_count[R + lane], agg_n);
+        }
+        __syncthreads();
+    } else {
+        // 1. per-rank / per-node counts of the channel
+        int rank_acc = 0, node_acc = 0;
+        for (int base = t0; base < t1; base += kNotifyThreads) {
+            const int t = base + tid;
+            const uint32_t m = t < t1 ? load_mask(in_rank + static_cast<int64_t>(t) * R, R) : 0u;
+            const uint32_t nm = node_bits(m, R, N);
+            for (int r = 0; r < R; ++r) {
+                const unsigned bb = __ballot_sync(0xffffffffu, (m >> r) & 1u);
+                if (lane == r) rank_acc += __popc(bb);
+            }
+            for (int n = 0; n < N; ++n) {
+                const unsigned bb = __ballot_sync(0xffffffffu, (nm >> n) & 1u);
+                if (lane == n) node_acc += __popc(bb);
+            }
+        }
+        if (lane < R && rank_acc) atomicAdd(&s_count[lane], rank_acc);
+        if (lane < N && node_acc) atomicAdd(&s_count[R + lane], node_acc);
+        __syncthreads();
+
+        // 2. publish the aggregate (the first channel of a source publishes its
+        //    inclusive prefix directly), then look back within the source rank
+        unsigned long long* mine = p.words + static_cast<int64_t>(b) * V;
+        if (tid < V && b != p.stall_block)
+            st_release_u64(mine + tid, pack_word(seq, c == 0 ? kFlagPrefix : kFlagAggregate,
+                                                 static_cast<uint32_t>(s_count[tid])));
+        __syncthreads();
+        bool timed_out = false;
+        const long long deadline = globaltimer_ns() + p.wait_limit_ns;
+        for (int v = warp; v < V; v += kNotifyWarps) {
+            const uint32_t ex = c == 0 ? 0u : segment_lookback(p, seq, b, s * C, v, lane, deadline, timed_out);
+            if (lane == 0) {
+                s_segex[v] = static_cast<int32_t>(ex);
+                if (c != 0 && b != p.stall_block)
+                    st_release_u64(mine + v, pack_word(seq, kFlagPrefix, ex + static_cast<uint32_t>(s_count[v])));
+            }
+        }
+        if (__any_sync(0xffffffffu, timed_out) && lane == 0) flag_error(p.a.status, EP_DEV_TIMEOUT);
+        __syncthreads();
+
     }
-    if (__any_sync(0xffffffffu, timed_out) && lane == 0) flag_error(p.a.status, EP_DEV_TIMEOUT);
-    __syncthreads();
 
     // 3. outputs of the block; the last channel checks the totals
     if (tid < V) {
@@ -337,14 +415,16 @@ size_t notify_workspace_bytes(const Shape& sh) {
     return kWorkspaceHeader + static_cast<size_t>(sh.R) * sh.C * V * sizeof(unsigned long long);
 }
 
-cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace, int stall_block,
-                          long long wait_limit_ns, cudaStream_t stream) {
-    const size_t ws_bytes = notify_workspace_bytes(sh);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes, stream);
-    if (e != cudaSuccess) return e;
+cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace, bool clear_workspace,
+                          bool force_lookback, int stall_block, long long wait_limit_ns,
+                          cudaStream_t stream) {
+    if (clear_workspace) {
+        const cudaError_t e = cudaMemsetAsync(workspace, 0, notify_workspace_bytes(sh), stream);
+        if (e != cudaSuccess) return e;
+    }
     NotifyKernelArgs p;
     p.a = a;
-    p.counters = static_cast<unsigned*>(workspace);
+    p.ticket = static_cast<unsigned long long*>(workspace);
     p.words = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + kWorkspaceHeader);
     p.R = sh.R;
     p.T = sh.T;
@@ -356,6 +436,10 @@ cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace,
     p.q = (sh.T + sh.C - 1) / sh.C;
     p.V = sh.R + sh.N;
     p.stall_block = stall_block;
+    // Small sources (a source's membership rows fit in 32 KB) recount earlier
+    // channels directly: no inter-block waits and no workspace traffic.
+    // force_lookback (the test hooks) keeps the lookback path on any shape.
+    p.recount = (!force_lookback && static_cast<long long>(sh.T) * sh.R <= 32 * 1024) ? 1 : 0;
     p.wait_limit_ns = wait_limit_ns;
     const size_t smem = sizeof(int32_t) * kNotifyThreads * static_cast<size_t>(sh.R + 1);
     const unsigned blocks = 1u + static_cast<unsigned>(sh.R * sh.C);

@@ -305,7 +305,8 @@ def alloc_layout(shape: EpShape, device="cuda") -> dict:
 def alloc_notify(shape: EpShape, device="cuda") -> dict:
     outs = {k: torch.empty(s, dtype=dt, device=device) for k, (s, dt) in notify_shapes(shape).items()}
     ws = ep_notify_workspace_bytes(shape)
-    outs["workspace"] = torch.empty((ws + 15) // 16 * 16, dtype=torch.uint8, device=device)
+    # zeroed once here; every notify call leaves it ready for the next one
+    outs["workspace"] = torch.zeros((ws + 15) // 16 * 16, dtype=torch.uint8, device=device)
     return outs
 
 

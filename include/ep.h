@@ -101,7 +101,7 @@ ep_status_t ep_check_shape(const ep_shape_t* shape);
 int32_t ep_num_nodes(const ep_shape_t* shape);
 
 /* Bytes of device scratch ep_notify_dispatch needs (its `workspace`), or 0
- * for an invalid shape. */
+ * for an invalid shape.  The workspace must be zero before its first use. */
 size_t ep_notify_workspace_bytes(const ep_shape_t* shape);
 
 /* ------------------------------------------------------------------------
@@ -135,8 +135,9 @@ ep_status_t ep_get_dispatch_layout(const ep_shape_t* shape, const int64_t* topk_
  * prefix) and sm0 stage 6 (per-rank prefix over global source rank, node
  * prefix, per-expert totals rounded up to expert_alignment); [RT]
  * intranodeNotifyDispatch / internodeNotifyDispatch for the outputs' names
- * and shapes.  One kernel: per (source rank, channel) block a count, then a
- * decoupled-lookback scan over the channels of the same source rank; the
+ * and shapes.  One kernel: per (source rank, channel) block a count and the
+ * prefix over the earlier channels of the same source rank (recounted
+ * directly for small sources, a decoupled-lookback scan otherwise); the
  * offset contributed by earlier source ranks comes from the per-rank counts,
  * as in the pages' notify.
  *
@@ -168,8 +169,12 @@ ep_status_t ep_get_dispatch_layout(const ep_shape_t* shape, const int64_t* topk_
  *                                                     recv_base[R] = total rows
  *   send_pos                   int32 [R src][T][R dst] row of (s,t) inside r's
  *                                                     region, or -1
- *   workspace                  device scratch of ep_notify_workspace_bytes();
- *                              cleared by this call, contents undefined after
+ *   workspace                  device scratch of ep_notify_workspace_bytes()
+ *                              bytes, zero-filled once before its first use
+ *                              (e.g. one cudaMemset); every call leaves it
+ *                              ready for the next, so it is never cleared
+ *                              again.  One workspace may serve calls of any
+ *                              shape in turn, but not two calls at once.
  *   host_num_recv_tokens       optional (may be NULL): int32 [R+1] in
  *                              host-mapped pinned memory (cudaHostAlloc with
  *                              cudaHostAllocMapped, or any device-visible
@@ -295,9 +300,10 @@ ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* 
 ep_status_t ep_sync_status(const int32_t* status, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
- * Testing hook for failure detection.  Runs ep_notify_dispatch with the
- * block at scan position `stall_block` withholding its published prefix and
- * every wait bounded by `wait_limit_us` microseconds.  The blocks that wait
+ * Testing hook for failure detection.  Runs ep_notify_dispatch on its
+ * lookback path (whatever the shape) with the block at scan position
+ * `stall_block` (-1: none) withholding its published prefix and every wait
+ * bounded by `wait_limit_us` microseconds.  The blocks that wait
  * on it give up, set EP_DEV_TIMEOUT and exit, so the context stays usable.
  * Output contents are undefined after such a run.
  */

@@ -291,3 +291,53 @@ def test_host_mapped_receive_counts():
     assert ep.ep_sync_status(status) == ep.EP_OK
     want = np.concatenate([nt_ref["num_recv_tokens"], [nt_ref["recv_base"][-1]]]).astype(np.int32)
     assert_equal("host_num_recv_tokens", host.numpy(), want)
+
+
+def test_workspace_reused_across_shapes_and_after_a_timeout():
+    """One notify workspace, zeroed once, serves calls of different shapes in
+    turn and stays valid after a call whose waits ran out."""
+    o = oracle.load()
+    shapes = [CONFIGS["low_latency"], CONFIGS["tiny"], EDGE["r32_min_hidden_repeats"], CONFIGS["low_latency"]]
+    biggest = max(ep.ep_notify_workspace_bytes(shape_of(w)) for w in shapes)
+    ws = torch.zeros(biggest, dtype=torch.uint8, device="cuda")
+    for i, w in enumerate(shapes):
+        idx, wt, x = make_inputs(w)
+        sh = shape_of(w)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        lay = ep.alloc_layout(sh)
+        nt = ep.alloc_notify(sh)
+        ep.ep_get_dispatch_layout(sh, idx.cuda(), lay["num_tokens_per_rank"], lay["num_tokens_per_rdma_rank"],
+                                  lay["num_tokens_per_expert"], lay["is_token_in_rank"], status)
+        args = (lay["is_token_in_rank"], lay["num_tokens_per_rank"], lay["num_tokens_per_rdma_rank"],
+                lay["num_tokens_per_expert"], nt)
+        if i == 1:  # a call that times out in the middle of the sequence
+            ep.ep_debug_notify_dispatch_stall(sh, *args, ws, status, stall_block=0, wait_limit_us=2000)
+            assert ep.ep_sync_status(status) == ep.EP_ERR_TIMEOUT
+            status.zero_()
+        ep.ep_notify_dispatch(sh, *args, ws, status)
+        assert ep.ep_sync_status(status) == ep.EP_OK
+        lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+        check_layout_notify(lay, nt, lay_ref, o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref))
+
+
+@pytest.mark.parametrize("name", ["tiny", "low_latency", "prefill", "channels_exceed_tokens", "odd_ranks_align",
+                                  "r32_min_hidden_repeats", "empty_tokens"])
+def test_notify_lookback_path_matches_oracle(name):
+    """Small sources normally take notify's recount path; the test hook forces
+    the inter-block lookback path on the same shapes, which must agree too."""
+    w = CONFIGS.get(name) or EDGE[name]
+    o = oracle.load()
+    idx, wt, x = make_inputs(w)
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay = ep.alloc_layout(sh)
+    nt = ep.alloc_notify(sh)
+    ep.ep_get_dispatch_layout(sh, idx.cuda(), lay["num_tokens_per_rank"], lay["num_tokens_per_rdma_rank"],
+                              lay["num_tokens_per_expert"], lay["is_token_in_rank"], status)
+    for _ in range(2):  # twice: the second call reuses the workspace state of the first
+        ep.ep_debug_notify_dispatch_stall(sh, lay["is_token_in_rank"], lay["num_tokens_per_rank"],
+                                          lay["num_tokens_per_rdma_rank"], lay["num_tokens_per_expert"], nt,
+                                          nt["workspace"], status, stall_block=-1, wait_limit_us=1000000)
+        assert ep.ep_sync_status(status) == ep.EP_OK
+        lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+        check_layout_notify(lay, nt, lay_ref, o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref))
