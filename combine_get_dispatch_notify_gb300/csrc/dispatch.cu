@@ -5,10 +5,14 @@
 // Persistent CTAs walk work units (token, row part) with a stride of the
 // grid.  Each CTA runs a shared-memory ring of `slots` buffers fed by the TMA
 // engine (bulk, non-tensor copies):
-//   warp 0 (producer): reads the unit's send_pos row (lane r = rank r),
-//        resolves the destination rows, waits for a free slot and issues one
-//        bulk global->shared copy of the row part, completing on the slot's
-//        "full" mbarrier;
+//   warp 0 (producer): issues the bulk global->shared copies of its first
+//        ring-full of row parts before waiting on notify (x is an input, so
+//        at small sizes all of x is in shared memory by the time the row map
+//        exists); then per unit reads the send_pos row (lane r = rank r),
+//        writes the destination rows into the slot descriptor and, for units
+//        beyond the first ring-full, waits for a free slot and issues the
+//        copy.  A slot's "full" mbarrier completes on two arrivals (copy
+//        armed, descriptor written) plus the copy's bytes;
 //   warp 1 (storer, one thread): waits "full", issues one bulk
 //        shared->global copy per destination, commits them as a bulk group,
 //        and frees the previous slot once its group has been read out;
@@ -69,10 +73,28 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     griddep_launch_dependents();
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], 2);  // arrivals: row part armed, descriptor written
             mbar_init(&empty[i], 1);
         }
         fence_mbarrier_init();
+    }
+    __syncthreads();
+    // x is an input of the step, not written by layout or notify, so the
+    // first ring-full of row parts is loaded while notify is still running.
+    const long long units_here =
+        blockIdx.x < p.num_units ? (p.num_units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int pre = units_here < S ? static_cast<int>(units_here) : S;
+    if (warp == 0 && lane == 0) {
+        long long u = blockIdx.x;
+        for (int i = 0; i < pre; ++i, u += gridDim.x) {
+            const long long g = u / p.parts;
+            const long long off = (u - g * p.parts) * static_cast<long long>(p.part_bytes);
+            const long long left = p.row_bytes - off;
+            const uint32_t bytes = left < p.part_bytes ? static_cast<uint32_t>(left) : p.part_bytes;
+            mbar_arrive_expect_tx(&full[i], bytes);
+            bulk_g2s(data + static_cast<size_t>(i) * p.part_bytes, p.x + g * p.row_bytes + off, bytes,
+                     &full[i]);
+        }
     }
     griddep_wait();  // send_pos / recv_base from notify are visible from here on
     if (tid <= p.R) base[tid] = p.recv_base[tid];
@@ -80,23 +102,29 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 
     if (warp == 0) {
         // ---------------- producer ----------------
-        int k = 0;  // phases armed so far (loads, then the end marker)
+        int k = 0;  // units (then the end marker) handed to the storer
         bool ok = true;
         for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             const long long g = u / p.parts;
             const int part = static_cast<int>(u - g * p.parts);
             const int32_t sp = lane < p.R ? __ldg(p.send_pos + g * p.R + lane) : -1;
             const unsigned valid = __ballot_sync(0xffffffffu, sp >= 0);
-            if (valid == 0u) continue;
             const int slot = k % S;
-            if (k >= S) {
+            const long long off = static_cast<long long>(part) * p.part_bytes;
+            const long long left = p.row_bytes - off;
+            const uint32_t bytes = left < p.part_bytes ? static_cast<uint32_t>(left) : p.part_bytes;
+            if (k >= pre) {  // not prefetched: wait for the slot, then load
                 bool got = true;
                 if (lane == 0)
                     got = mbar_wait(&empty[slot], ((k / S) - 1) & 1, globaltimer_ns() + p.wait_limit_ns);
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
                     ok = false;
                     break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    bulk_g2s(data + static_cast<size_t>(slot) * p.part_bytes, p.x + g * p.row_bytes + off,
+                             bytes, &full[slot]);
                 }
             }
             if (sp >= 0) {
@@ -110,31 +138,24 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                 }
                 desc[slot].rows[__popc(valid & lanemask_lt())] = row;
             }
-            const long long off = static_cast<long long>(part) * p.part_bytes;
-            const long long left = p.row_bytes - off;
-            const uint32_t bytes = left < p.part_bytes ? static_cast<uint32_t>(left) : p.part_bytes;
             if (lane == 0) {
                 desc[slot].n = __popc(valid);
                 desc[slot].bytes = bytes;
                 desc[slot].part_off = off;
             }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&full[slot], bytes);
-                bulk_g2s(data + static_cast<size_t>(slot) * p.part_bytes, p.x + g * p.row_bytes + off,
-                         bytes, &full[slot]);
-            }
+            __syncwarp();  // every lane's descriptor writes precede the release below
+            if (lane == 0) mbar_arrive(&full[slot]);
             ++k;
         }
-        if (ok) {  // end-of-stream marker
+        if (ok) {  // end-of-stream marker (both arrivals, no data)
             const int slot = k % S;
             bool got = true;
             if (k >= S && lane == 0)
                 got = mbar_wait(&empty[slot], ((k / S) - 1) & 1, globaltimer_ns() + p.wait_limit_ns);
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (got) {
+            if (__shfl_sync(0xffffffffu, got, 0)) {
                 if (lane == 0) {
                     desc[slot].n = -1;
+                    mbar_arrive(&full[slot]);
                     mbar_arrive(&full[slot]);
                 }
                 ++k;
@@ -145,7 +166,9 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         if (lane == 0) {
             if (!ok) flag_error(p.status, EP_DEV_TIMEOUT);
             // Drain: the newest phase armed on each slot has completed, so no
-            // bulk copy into shared memory outlives the CTA.
+            // bulk copy into shared memory outlives the CTA.  (A wait can only
+            // run out after every prefetched unit was handed over, so no phase
+            // is left with one arrival.)
             for (int x = 0; x < S; ++x) {
                 const int phases = k > x ? (k - x + S - 1) / S : 0;
                 if (phases > 0 &&

@@ -436,10 +436,10 @@ cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace,
     p.q = (sh.T + sh.C - 1) / sh.C;
     p.V = sh.R + sh.N;
     p.stall_block = stall_block;
-    // Small sources (a source's membership rows fit in 32 KB) recount earlier
+    // Small sources (a source's membership rows fit in 8 KB) recount earlier
     // channels directly: no inter-block waits and no workspace traffic.
     // force_lookback (the test hooks) keeps the lookback path on any shape.
-    p.recount = (!force_lookback && static_cast<long long>(sh.T) * sh.R <= 32 * 1024) ? 1 : 0;
+    p.recount = (!force_lookback && static_cast<long long>(sh.T) * sh.R <= 8 * 1024) ? 1 : 0;
     p.wait_limit_ns = wait_limit_ns;
     const size_t smem = sizeof(int32_t) * kNotifyThreads * static_cast<size_t>(sh.R + 1);
     const unsigned blocks = 1u + static_cast<unsigned>(sh.R * sh.C);

@@ -255,6 +255,12 @@ ep_status_t ep_notify_dispatch_noalloc(
  *                      expert lives on r, else 0
  *   recv_src_info  out int32 [capacity_rows][2]  (source rank, source token)
  * Rows beyond recv_base[R] are left untouched.
+ * Kernels of this library overlap their launch with the preceding kernel in
+ * the stream (programmatic dependent launch), and ep_dispatch starts reading
+ * x before that kernel has finished; it waits for the row map before writing
+ * anything.  So x must be complete by the time the step's kernels start,
+ * which holds for any producer enqueued earlier in the stream unless that
+ * producer itself releases its dependents early (griddepcontrol).
  */
 ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
                         const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
