@@ -205,9 +205,12 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         }
     } else {
         // ---------------- metadata ----------------
+        // (cached mode passes no top-k arrays; recv_src_info may be omitted too)
+        const bool with_topk = p.recv_topk_idx != nullptr;
+        const bool with_src = p.recv_src_info != nullptr;
         const int mw = warp - 2;
         int i = 0;
-        for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        for (long long u = blockIdx.x; (with_topk || with_src) && u < p.num_units; u += gridDim.x) {
             if (u % p.parts != 0) continue;
             if ((i++ & 1) != mw) continue;
             const long long g = u / p.parts;
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
             long long e = -1;
             float w = 0.0f;
             int owner = -1;
-            if (lane < p.K) {
+            if (with_topk && lane < p.K) {
                 e = __ldg(p.topk_idx + g * p.K + lane);
                 w = __ldg(p.topk_w + g * p.K + lane);
                 owner = e >= 0 ? static_cast<int>(e / p.E_loc) : -1;
@@ -227,12 +230,12 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                 m &= m - 1;
                 const long long row = base[r] + __shfl_sync(0xffffffffu, sp, r);
                 if (row >= p.capacity || row >= base[r + 1]) continue;
-                if (lane < p.K) {
+                if (with_topk && lane < p.K) {
                     const bool here = owner == r;
                     p.recv_topk_idx[row * p.K + lane] = here ? e - static_cast<long long>(r) * p.E_loc : -1;
                     p.recv_topk_w[row * p.K + lane] = here ? w : 0.0f;
                 }
-                if (lane == 0) *reinterpret_cast<int2*>(p.recv_src_info + row * 2) = make_int2(s, t);
+                if (with_src && lane == 0) *reinterpret_cast<int2*>(p.recv_src_info + row * 2) = make_int2(s, t);
             }
         }
     }

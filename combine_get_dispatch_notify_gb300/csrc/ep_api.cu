@@ -226,11 +226,18 @@ ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_
     if (capacity_rows < 0) return EP_ERR_INVALID_ARG;
     const long long tokens = static_cast<long long>(sh.R) * sh.T;
     const long long cap = capacity_rows;
-    if (!ep::array_ok(x, tokens * sh.H, 16) || !ep::array_ok(topk_idx, tokens * sh.K, 8) ||
-        !ep::array_ok(topk_w, tokens * sh.K, 4) || !ep::array_ok(send_pos, tokens * sh.R, 4) ||
+    // Cached mode ([RT] intranodeDispatch with cachedMode): the four top-k
+    // arrays are all NULL and only rows (and optionally source info) move.
+    const bool topk_given = topk_idx != nullptr || topk_w != nullptr || recv_topk_idx != nullptr ||
+                            recv_topk_w != nullptr;
+    if (topk_given && (!ep::array_ok(topk_idx, tokens * sh.K, 8) || !ep::array_ok(topk_w, tokens * sh.K, 4) ||
+                       !ep::array_ok(recv_topk_idx, cap * sh.K, 8) || !ep::array_ok(recv_topk_w, cap * sh.K, 4) ||
+                       (tokens > 0 && (topk_idx == nullptr || topk_w == nullptr)) ||
+                       (cap > 0 && (recv_topk_idx == nullptr || recv_topk_w == nullptr))))
+        return EP_ERR_INVALID_ARG;
+    if (!ep::array_ok(x, tokens * sh.H, 16) || !ep::array_ok(send_pos, tokens * sh.R, 4) ||
         !ep::aligned8(recv_base) || !ep::array_ok(recv_x, cap * sh.H, 16) ||
-        !ep::array_ok(recv_topk_idx, cap * sh.K, 8) || !ep::array_ok(recv_topk_w, cap * sh.K, 4) ||
-        !ep::array_ok(recv_src_info, cap * 2, 8) || !ep::aligned4(status))
+        (recv_src_info != nullptr && !ep::aligned8(recv_src_info)) || !ep::aligned4(status))
         return EP_ERR_INVALID_ARG;
     return ep::from_cuda(ep::launch_dispatch(sh, x, topk_idx, topk_w, send_pos, recv_base,
                                              capacity_rows, recv_x, recv_topk_idx, recv_topk_w,

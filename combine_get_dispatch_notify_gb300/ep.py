@@ -258,18 +258,20 @@ def ep_debug_notify_dispatch_stall(shape: EpShape, is_token_in_rank, num_tokens_
 
 def ep_dispatch(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x, recv_topk_idx,
                 recv_topk_w, recv_src_info, status, stream=None) -> None:
+    """Cached mode: pass topk_idx, topk_w, recv_topk_idx and recv_topk_w as None
+    (and recv_src_info optionally) to reuse an earlier notify handle."""
     R, T, K, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.hidden
     cap = _rows(recv_x, "recv_x")
     rc = lib().ep_dispatch(
         ctypes.byref(shape), _t(x, torch.bfloat16, (R, T, H), "x"),
-        _t(topk_idx, torch.int64, (R, T, K), "topk_idx"),
-        _t(topk_w, torch.float32, (R, T, K), "topk_w"),
+        _t(topk_idx, torch.int64, (R, T, K), "topk_idx", nullable=True),
+        _t(topk_w, torch.float32, (R, T, K), "topk_w", nullable=True),
         _t(send_pos, torch.int32, (R, T, R), "send_pos"),
         _t(recv_base, torch.int64, (R + 1,), "recv_base"), _i64(cap),
         _t(recv_x, torch.bfloat16, (cap, H), "recv_x"),
-        _t(recv_topk_idx, torch.int64, (cap, K), "recv_topk_idx"),
-        _t(recv_topk_w, torch.float32, (cap, K), "recv_topk_w"),
-        _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info"),
+        _t(recv_topk_idx, torch.int64, (cap, K), "recv_topk_idx", nullable=True),
+        _t(recv_topk_w, torch.float32, (cap, K), "recv_topk_w", nullable=True),
+        _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info", nullable=True),
         _t(status, torch.int32, (1,), "status"), _stream(stream))
     _check("ep_dispatch", rc)
 
@@ -354,3 +356,14 @@ class Pipeline:
                    Nt["send_pos"], Nt["recv_base"], C["combined_x"], C["combined_w"], self.status,
                    stream)
         return C["combined_x"], C["combined_w"]
+
+    def run_cached(self, x, y=None, stream=None):
+        """Cached mode: dispatch and combine only, reusing the handle (send_pos,
+        recv_base) of the last :meth:`run`; the top-k is not dispatched and the
+        combined weights are not produced."""
+        sh, Nt, D, C = self.shape, self.notify, self.dispatch, self.combine
+        ep_dispatch(sh, x, None, None, Nt["send_pos"], Nt["recv_base"], D["recv_x"], None, None, None,
+                    self.status, stream)
+        ep_combine(sh, D["recv_x"] if y is None else y, None, Nt["send_pos"], Nt["recv_base"],
+                   C["combined_x"], None, self.status, stream)
+        return C["combined_x"]

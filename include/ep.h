@@ -255,6 +255,12 @@ ep_status_t ep_notify_dispatch_noalloc(
  *                      expert lives on r, else 0
  *   recv_src_info  out int32 [capacity_rows][2]  (source rank, source token)
  * Rows beyond recv_base[R] are left untouched.
+ * Cached mode ([RT] intranodeDispatch / internodeDispatch with cachedMode,
+ * where the top-k is not dispatched): a handle (send_pos, recv_base) from an
+ * earlier ep_notify_dispatch stays valid for any later step with the same
+ * routing, so layout and notify can be skipped.  Pass topk_idx, topk_w,
+ * recv_topk_idx and recv_topk_w all as NULL to move only the rows;
+ * recv_src_info may be NULL in any mode.
  * Kernels of this library overlap their launch with the preceding kernel in
  * the stream (programmatic dependent launch), and ep_dispatch starts reading
  * x before that kernel has finished; it waits for the row map before writing

@@ -120,8 +120,10 @@ class Oracle:
         return out
 
     # -- step 3 --------------------------------------------------------------------
-    def dispatch(self, R, T, K, E, H, C, x, topk_idx, topk_w, send_pos, recv_base, payload=True):
-        """Dispatch; ``payload=False`` computes only the metadata rows."""
+    def dispatch(self, R, T, K, E, H, C, x, topk_idx, topk_w, send_pos, recv_base, payload=True,
+                 with_topk=True):
+        """Dispatch; ``payload=False`` computes only the metadata rows;
+        ``with_topk=False`` is cached mode (no top-k fields)."""
         rows = int(recv_base[-1])
         topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
         topk_w = np.ascontiguousarray(topk_w, dtype=np.float32)
@@ -129,8 +131,8 @@ class Oracle:
         recv_base = np.ascontiguousarray(recv_base, dtype=np.int64)
         out = dict(
             recv_x=np.zeros((rows, H), np.uint16) if payload else None,
-            recv_topk_idx=np.zeros((rows, K), np.int64),
-            recv_topk_w=np.zeros((rows, K), np.float32),
+            recv_topk_idx=np.zeros((rows, K), np.int64) if with_topk else None,
+            recv_topk_w=np.zeros((rows, K), np.float32) if with_topk else None,
             recv_src_info=np.zeros((rows, 2), np.int32),
         )
         xs = np.ascontiguousarray(x, dtype=np.uint16) if payload else None

@@ -285,22 +285,27 @@ static int dispatch_token(int R, int T, int K, int E, int H, int s, int t,
         int64_t row = recv_base[r] + pos;
         if (row >= recv_base[r + 1]) return -1; /* row outside r's region */
         if (recv_x && x_row) memcpy(recv_x + (size_t)row * H, x_row, sizeof(uint16_t) * (size_t)H);
-        for (int k = 0; k < K; ++k) {
+        for (int k = 0; recv_topk_idx && k < K; ++k) { /* cached mode: no top-k */
             int64_t e = topk_idx[((size_t)s * T + t) * K + k];
             int here = e >= 0 && e / E_loc == r;
             recv_topk_idx[(size_t)row * K + k] = here ? e - (MUT(6) ? 0 : (int64_t)r * E_loc) : -1;
             recv_topk_w[(size_t)row * K + k] = here ? topk_w[((size_t)s * T + t) * K + k] : 0.0f;
         }
-        recv_src_info[(size_t)row * 2 + 0] = s;
-        recv_src_info[(size_t)row * 2 + 1] = t;
+        if (recv_src_info) {
+            recv_src_info[(size_t)row * 2 + 0] = s;
+            recv_src_info[(size_t)row * 2 + 1] = t;
+        }
     }
     return 0;
 }
 
 /* Whole dispatch in the pages' order: source rank, channel, token.  x and
  * recv_x may both be NULL to produce only the metadata (for shapes whose
- * payload does not fit in host memory).  Returns -1 when a row falls outside
- * its destination's region. */
+ * payload does not fit in host memory).  In cached mode ([RT]
+ * intranodeDispatch with cachedMode, num_experts 0) the top-k is not
+ * dispatched: recv_topk_idx / recv_topk_w are NULL, and recv_src_info may be
+ * NULL as well.  Returns -1 when a row falls outside its destination's
+ * region. */
 int oracle_dispatch(int R, int T, int K, int E, int H, int C,
                     const uint16_t* x,        /* [R][T][H] or NULL */
                     const int64_t* topk_idx,  /* [R][T][K] */

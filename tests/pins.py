@@ -353,9 +353,21 @@ def check_bf16_rounding(o):
     assert np.isnan(bf16_bits_to_f32(got[nan])).all()
 
 
+def check_dispatch_cached_mode(o):
+    """Cached mode moves the same rows and source info, without top-k fields."""
+    for sh in SHAPES[:4]:
+        w, idx, wt, x = make_case(**sh)
+        lay, nt, dp = run(o, w, idx, wt, x)
+        cached = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, x, idx, wt, nt["send_pos"], nt["recv_base"],
+                            with_topk=False)
+        assert cached["recv_topk_idx"] is None and cached["recv_topk_w"] is None
+        np.testing.assert_array_equal(cached["recv_x"], dp["recv_x"])
+        np.testing.assert_array_equal(cached["recv_src_info"], dp["recv_src_info"])
+
+
 ALL_CHECKS = [
     check_hand_worked, check_channel_ranges_hand, check_layout_library, check_notify_library,
     check_channel_independence, check_dispatch_stable_sort, check_dispatch_counting_sort,
     check_dispatch_identity_rank, check_dispatch_topk_fields, check_combine_identity_closed_form,
-    check_combine_error_bound, check_combine_order, check_bf16_rounding,
+    check_combine_error_bound, check_combine_order, check_bf16_rounding, check_dispatch_cached_mode,
 ]

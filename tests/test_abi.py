@@ -112,6 +112,11 @@ def test_invalid_calls_return_before_touching_the_device(ep):
                          fake, fake, fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
     assert L.ep_dispatch(ctypes.byref(good), odd, fake, fake, fake, fake, ctypes.c_int64(8), fake,
                          fake, fake, fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
+    # top-k arrays are all-or-none (none = cached mode)
+    assert L.ep_dispatch(ctypes.byref(good), fake, fake, vp(None), fake, fake, ctypes.c_int64(8), fake,
+                         fake, fake, fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch(ctypes.byref(good), fake, fake, fake, fake, fake, ctypes.c_int64(8), fake,
+                         vp(None), vp(None), fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
     assert L.ep_combine(ctypes.byref(good), vp(None), vp(None), 4, fake, fake, fake, vp(None), fake,
                         vp(0)) == ep.EP_ERR_INVALID_ARG  # y missing
     assert L.ep_combine(ctypes.byref(good), fake, vp(None), 4, fake, fake, fake, fake, fake,

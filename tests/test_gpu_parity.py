@@ -341,3 +341,35 @@ def test_notify_lookback_path_matches_oracle(name):
         assert ep.ep_sync_status(status) == ep.EP_OK
         lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
         check_layout_notify(lay, nt, lay_ref, o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref))
+
+
+
+@pytest.mark.parametrize("name", ["low_latency", "r32_min_hidden_repeats", "all_masked"])
+def test_cached_mode_reuses_the_handle(name):
+    """Cached mode: a handle from one full step serves a later step with the same
+    routing and new activations; only rows move, combine matches the oracle."""
+    w = CONFIGS.get(name) or EDGE[name]
+    o = oracle.load()
+    idx, wt, x1 = make_inputs(w)
+    x2 = gen_x_seeded(w, 99)
+    pipe = ep.Pipeline(shape_of(w), max(1, worst_case_rows(w)))
+    pipe.run(x1.cuda(), idx.cuda(), wt.cuda())
+    assert ep.ep_sync_status(pipe.status) == ep.EP_OK
+    src_before = pipe.dispatch["recv_src_info"].clone()
+    cx = pipe.run_cached(x2.cuda())
+    assert ep.ep_sync_status(pipe.status) == ep.EP_OK
+    xb = x2.view(torch.int16).numpy().view(np.uint16)
+    lay = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+    nt = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay)
+    dp = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, xb, idx.numpy(), wt.numpy(), nt["send_pos"], nt["recv_base"],
+                    with_topk=False)
+    rows = int(nt["recv_base"][-1])
+    assert_equal("recv_x (cached)", u16(pipe.dispatch["recv_x"][:rows]), dp["recv_x"])
+    assert torch.equal(src_before, pipe.dispatch["recv_src_info"])  # not rewritten
+    cb = o.combine(w.R, w.T, w.K, w.H, dp["recv_x"], None, nt["send_pos"], nt["recv_base"])
+    assert_combine_close("combined_x (cached)", u16(cx), cb["combined_x"])
+
+
+def gen_x_seeded(w, seed):
+    from combine_get_dispatch_notify_gb300.workloads import gen_x
+    return gen_x(w.replace(seed=seed))
