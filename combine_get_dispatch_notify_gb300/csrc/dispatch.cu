@@ -52,6 +52,9 @@ struct DispatchArgs {
     int64_t* recv_topk_idx;
     float* recv_topk_w;
     int32_t* recv_src_info;
+    const float* x_scales;   // [R*T][num_scales] or NULL (FP8 rows)
+    float* recv_x_scales;    // [capacity][num_scales] or NULL
+    int num_scales;
     int32_t* status;
     int R, T, K, E_loc, parts, slots;
     uint32_t part_bytes;
@@ -208,9 +211,11 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         // (cached mode passes no top-k arrays; recv_src_info may be omitted too)
         const bool with_topk = p.recv_topk_idx != nullptr;
         const bool with_src = p.recv_src_info != nullptr;
+        const bool with_scales = p.recv_x_scales != nullptr;
         const int mw = warp - 2;
         int i = 0;
-        for (long long u = blockIdx.x; (with_topk || with_src) && u < p.num_units; u += gridDim.x) {
+        for (long long u = blockIdx.x; (with_topk || with_src || with_scales) && u < p.num_units;
+             u += gridDim.x) {
             if (u % p.parts != 0) continue;
             if ((i++ & 1) != mw) continue;
             const long long g = u / p.parts;
@@ -236,6 +241,9 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                     p.recv_topk_w[row * p.K + lane] = here ? w : 0.0f;
                 }
                 if (with_src && lane == 0) *reinterpret_cast<int2*>(p.recv_src_info + row * 2) = make_int2(s, t);
+                if (with_scales)  // the token's FP8 block scales travel with its row
+                    for (int j = lane; j < p.num_scales; j += kWarp)
+                        p.recv_x_scales[row * p.num_scales + j] = __ldg(p.x_scales + g * p.num_scales + j);
             }
         }
     }
@@ -243,9 +251,10 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 
 }  // namespace
 
-cudaError_t launch_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
-                            const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
-                            int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, const float* x_scales,
+                            int num_scales, const int64_t* topk_idx, const float* topk_w,
+                            const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
+                            void* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
                             cudaStream_t stream) {
     const long long tokens = static_cast<long long>(sh.R) * sh.T;
@@ -253,7 +262,7 @@ cudaError_t launch_dispatch(const Shape& sh, const uint16_t* x, const int64_t* t
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const long long grid_target = static_cast<long long>(sms) * kCtasPerSm;
-    const long long row_bytes = sh.row_bytes();
+    const long long row_bytes = static_cast<long long>(sh.H) * x_elem_bytes;
 
     // Row parts: at most 32 KB, and split further (down to 2 KB) while there
     // are fewer than 8 units per CTA.  Parts are multiples of 16 bytes.
@@ -265,13 +274,16 @@ cudaError_t launch_dispatch(const Shape& sh, const uint16_t* x, const int64_t* t
     slots = slots < 2 ? 2 : (slots > kMaxSlots ? kMaxSlots : slots);
 
     DispatchArgs p;
-    p.x = reinterpret_cast<const uint8_t*>(x);
+    p.x = static_cast<const uint8_t*>(x);
+    p.x_scales = x_scales;
+    p.recv_x_scales = recv_x_scales;
+    p.num_scales = num_scales;
     p.topk_idx = topk_idx;
     p.topk_w = topk_w;
     p.send_pos = send_pos;
     p.recv_base = recv_base;
     p.capacity = capacity_rows;
-    p.recv_x = reinterpret_cast<uint8_t*>(recv_x);
+    p.recv_x = static_cast<uint8_t*>(recv_x);
     p.recv_topk_idx = recv_topk_idx;
     p.recv_topk_w = recv_topk_w;
     p.recv_src_info = recv_src_info;

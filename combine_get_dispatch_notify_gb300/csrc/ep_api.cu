@@ -239,9 +239,41 @@ ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_
         !ep::aligned8(recv_base) || !ep::array_ok(recv_x, cap * sh.H, 16) ||
         (recv_src_info != nullptr && !ep::aligned8(recv_src_info)) || !ep::aligned4(status))
         return EP_ERR_INVALID_ARG;
-    return ep::from_cuda(ep::launch_dispatch(sh, x, topk_idx, topk_w, send_pos, recv_base,
-                                             capacity_rows, recv_x, recv_topk_idx, recv_topk_w,
+    return ep::from_cuda(ep::launch_dispatch(sh, x, 2, nullptr, 0, topk_idx, topk_w, send_pos, recv_base,
+                                             capacity_rows, recv_x, nullptr, recv_topk_idx, recv_topk_w,
                                              recv_src_info, status, stream));
+}
+
+ep_status_t ep_dispatch_fp8(const ep_shape_t* shape, const uint8_t* x, const float* x_scales,
+                            int32_t num_scales, const int64_t* topk_idx, const float* topk_w,
+                            const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
+                            uint8_t* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
+                            float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                            cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    if (capacity_rows < 0 || sh.H % 16 != 0 || num_scales < 0 || num_scales > 4096) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    const long long cap = capacity_rows;
+    const bool topk_given = topk_idx != nullptr || topk_w != nullptr || recv_topk_idx != nullptr ||
+                            recv_topk_w != nullptr;
+    if (topk_given && (!ep::array_ok(topk_idx, tokens * sh.K, 8) || !ep::array_ok(topk_w, tokens * sh.K, 4) ||
+                       !ep::array_ok(recv_topk_idx, cap * sh.K, 8) || !ep::array_ok(recv_topk_w, cap * sh.K, 4) ||
+                       (tokens > 0 && (topk_idx == nullptr || topk_w == nullptr)) ||
+                       (cap > 0 && (recv_topk_idx == nullptr || recv_topk_w == nullptr))))
+        return EP_ERR_INVALID_ARG;
+    if (num_scales > 0 && (!ep::array_ok(x_scales, tokens * num_scales, 4) ||
+                           !ep::array_ok(recv_x_scales, cap * num_scales, 4) ||
+                           (tokens > 0 && x_scales == nullptr) || (cap > 0 && recv_x_scales == nullptr)))
+        return EP_ERR_INVALID_ARG;
+    if (!ep::array_ok(x, tokens * sh.H, 16) || !ep::array_ok(send_pos, tokens * sh.R, 4) ||
+        !ep::aligned8(recv_base) || !ep::array_ok(recv_x, cap * sh.H, 16) ||
+        (recv_src_info != nullptr && !ep::aligned8(recv_src_info)) || !ep::aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    return ep::from_cuda(ep::launch_dispatch(sh, x, 1, num_scales > 0 ? x_scales : nullptr, num_scales,
+                                             topk_idx, topk_w, send_pos, recv_base, capacity_rows, recv_x,
+                                             num_scales > 0 ? recv_x_scales : nullptr, recv_topk_idx,
+                                             recv_topk_w, recv_src_info, status, stream));
 }
 
 ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* y_w,

@@ -59,9 +59,12 @@ cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace,
                           bool force_lookback, int stall_block, long long wait_limit_ns,
                           cudaStream_t stream);
 
-cudaError_t launch_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
-                            const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
-                            int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+// x rows are H * x_elem_bytes bytes (2: bf16, 1: FP8); x_scales /
+// recv_x_scales ([tokens|rows][num_scales] fp32) may be NULL.
+cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, const float* x_scales,
+                            int num_scales, const int64_t* topk_idx, const float* topk_w,
+                            const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
+                            void* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
                             cudaStream_t stream);
 

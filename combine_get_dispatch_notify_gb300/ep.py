@@ -72,6 +72,8 @@ _SIGS = {
     "ep_get_dispatch_layout": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 6 + [_vp]),
     "ep_notify_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_sz, _vp, _vp, _vp]),
     "ep_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 5 + [_vp]),
+    "ep_dispatch_fp8": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i32] + [_vp] * 4 + [_i64] +
+                        [_vp] * 6 + [_vp]),
     "ep_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i64] + [_vp] * 5 + [_vp]),
     "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 15 + [_vp, _vp, _vp]),
     "ep_sync_status": (_i32, [_vp, _vp]),
@@ -274,6 +276,29 @@ def ep_dispatch(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x
         _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info", nullable=True),
         _t(status, torch.int32, (1,), "status"), _stream(stream))
     _check("ep_dispatch", rc)
+
+
+def ep_dispatch_fp8(shape: EpShape, x, x_scales, topk_idx, topk_w, send_pos, recv_base, recv_x,
+                    recv_x_scales, recv_topk_idx, recv_topk_w, recv_src_info, status, stream=None) -> None:
+    """FP8 rows (uint8 e4m3 bytes, H per token) plus per-token fp32 scales
+    ([..., num_scales]; None for none).  Top-k and source info as in ep_dispatch."""
+    R, T, K, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.hidden
+    cap = _rows(recv_x, "recv_x")
+    S = 0 if x_scales is None else x_scales.shape[-1]
+    rc = lib().ep_dispatch_fp8(
+        ctypes.byref(shape), _t(x, torch.uint8, (R, T, H), "x"),
+        _t(x_scales, torch.float32, (R, T, S), "x_scales", nullable=True), _i32(S),
+        _t(topk_idx, torch.int64, (R, T, K), "topk_idx", nullable=True),
+        _t(topk_w, torch.float32, (R, T, K), "topk_w", nullable=True),
+        _t(send_pos, torch.int32, (R, T, R), "send_pos"),
+        _t(recv_base, torch.int64, (R + 1,), "recv_base"), _i64(cap),
+        _t(recv_x, torch.uint8, (cap, H), "recv_x"),
+        _t(recv_x_scales, torch.float32, (cap, S), "recv_x_scales", nullable=True),
+        _t(recv_topk_idx, torch.int64, (cap, K), "recv_topk_idx", nullable=True),
+        _t(recv_topk_w, torch.float32, (cap, K), "recv_topk_w", nullable=True),
+        _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info", nullable=True),
+        _t(status, torch.int32, (1,), "status"), _stream(stream))
+    _check("ep_dispatch_fp8", rc)
 
 
 def ep_combine(shape: EpShape, y, y_w, send_pos, recv_base, combined_x, combined_w, status,

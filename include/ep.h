@@ -275,6 +275,29 @@ ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_
                         cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Step 3, FP8 rows.  [RT] intranodeDispatch / internodeDispatch take x with
+ * an element size of 1 byte plus x_scales (num_scales fp32 per token) and
+ * return recv_x_scales beside recv_x; the FP8 scale buffer is one of the
+ * per-channel buffers sized in their asserts.  Same placement, top-k and
+ * cached-mode rules as ep_dispatch; rows are H bytes (H % 16 == 0 here).
+ * The bytes are copied as they are: quantising to and from e4m3 is the
+ * caller's (the expert's) job.
+ *
+ *   x              in  uint8 [R][T][H]              FP8 (e4m3) activations
+ *   x_scales       in  fp32  [R][T][num_scales]     or NULL when num_scales == 0
+ *   num_scales     0 .. 4096 scales per token (for example one per 128 elements)
+ *   recv_x         out uint8 [capacity_rows][H]
+ *   recv_x_scales  out fp32  [capacity_rows][num_scales] (or NULL when 0)
+ * other arguments as in ep_dispatch.
+ */
+ep_status_t ep_dispatch_fp8(const ep_shape_t* shape, const uint8_t* x, const float* x_scales,
+                            int32_t num_scales, const int64_t* topk_idx, const float* topk_w,
+                            const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
+                            uint8_t* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
+                            float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                            cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Step 4 - combine.  [RT] intranodeCombine / internodeCombine (combined_x is
  * bf16, combined_topk_weights fp32), [AR] 4.2 (each received row returns to
  * its (src_rank, src_idx)).  For every source token (s,t):

@@ -55,8 +55,8 @@ class Oracle:
 
     def __init__(self, path: str):
         self.lib = ctypes.CDLL(path)
-        for fn in ("oracle_layout", "oracle_notify", "oracle_dispatch", "oracle_combine",
-                   "oracle_num_nodes"):
+        for fn in ("oracle_layout", "oracle_notify", "oracle_dispatch", "oracle_dispatch_fp8",
+                   "oracle_combine", "oracle_num_nodes"):
             getattr(self.lib, fn).restype = ctypes.c_int
         self.lib.oracle_f32_to_bf16.restype = None
 
@@ -142,6 +142,32 @@ class Oracle:
                                       _p(out["recv_src_info"]))
         if rc != 0:
             raise ValueError("oracle_dispatch: a row falls outside its destination region")
+        return out
+
+    def dispatch_fp8(self, R, T, K, E, H, C, x, x_scales, topk_idx, topk_w, send_pos, recv_base,
+                     with_topk=True):
+        """FP8 dispatch: byte rows (H per token) plus their fp32 scales rows."""
+        rows = int(recv_base[-1])
+        S = 0 if x_scales is None else int(x_scales.shape[-1])
+        x = np.ascontiguousarray(x, dtype=np.uint8)
+        xs = None if x_scales is None else np.ascontiguousarray(x_scales, dtype=np.float32)
+        ti = np.ascontiguousarray(topk_idx, dtype=np.int64) if with_topk else None
+        tw = np.ascontiguousarray(topk_w, dtype=np.float32) if with_topk else None
+        out = dict(
+            recv_x=np.zeros((rows, H), np.uint8),
+            recv_x_scales=np.zeros((rows, S), np.float32) if S else None,
+            recv_topk_idx=np.zeros((rows, K), np.int64) if with_topk else None,
+            recv_topk_w=np.zeros((rows, K), np.float32) if with_topk else None,
+            recv_src_info=np.zeros((rows, 2), np.int32),
+        )
+        rc = self.lib.oracle_dispatch_fp8(R, T, K, E, H, C, S, _p(x), _p(xs), _p(ti), _p(tw),
+                                          _p(np.ascontiguousarray(send_pos, dtype=np.int32)),
+                                          _p(np.ascontiguousarray(recv_base, dtype=np.int64)),
+                                          _p(out["recv_x"]), _p(out["recv_x_scales"]),
+                                          _p(out["recv_topk_idx"]), _p(out["recv_topk_w"]),
+                                          _p(out["recv_src_info"]))
+        if rc != 0:
+            raise ValueError("oracle_dispatch_fp8: a row falls outside its destination region")
         return out
 
     # -- step 4 --------------------------------------------------------------------

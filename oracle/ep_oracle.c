@@ -272,11 +272,12 @@ int oracle_notify(int R, int T, int E, int C, int expert_alignment,
  * recv_topk_idx (int64), recv_topk_weights (fp32) and the source index / meta;
  * [AR] 4.1 gives src_info as {src_rank, src_idx} (P4).  Readings P5 for the
  * top-k fields.  Rows land at recv_base[r] + send_pos[s][t][r]. */
-static int dispatch_token(int R, int T, int K, int E, int H, int s, int t,
-                           const uint16_t* x_row, const int64_t* topk_idx, const float* topk_w,
-                           const int32_t* send_pos, const int64_t* recv_base,
-                           uint16_t* recv_x, int64_t* recv_topk_idx, float* recv_topk_w,
-                           int32_t* recv_src_info)
+static int dispatch_token(int R, int T, int K, int E, size_t row_bytes, int s, int t,
+                          const void* x_row, const float* scales_row, int S,
+                          const int64_t* topk_idx, const float* topk_w,
+                          const int32_t* send_pos, const int64_t* recv_base,
+                          void* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
+                          float* recv_topk_w, int32_t* recv_src_info)
 {
     const int E_loc = E / R;
     for (int r = 0; r < R; ++r) {
@@ -284,7 +285,9 @@ static int dispatch_token(int R, int T, int K, int E, int H, int s, int t,
         if (pos < 0) continue;
         int64_t row = recv_base[r] + pos;
         if (row >= recv_base[r + 1]) return -1; /* row outside r's region */
-        if (recv_x && x_row) memcpy(recv_x + (size_t)row * H, x_row, sizeof(uint16_t) * (size_t)H);
+        if (recv_x && x_row) memcpy((uint8_t*)recv_x + (size_t)row * row_bytes, x_row, row_bytes);
+        if (recv_x_scales && scales_row)
+            memcpy(recv_x_scales + (size_t)row * S, scales_row, sizeof(float) * (size_t)S);
         for (int k = 0; recv_topk_idx && k < K; ++k) { /* cached mode: no top-k */
             int64_t e = topk_idx[((size_t)s * T + t) * K + k];
             int here = e >= 0 && e / E_loc == r;
@@ -322,8 +325,41 @@ int oracle_dispatch(int R, int T, int K, int E, int H, int C,
             int b, e;
             channel_range(T, C, c, &b, &e);
             for (int t = b; t < e; ++t)
-                if (dispatch_token(R, T, K, E, H, s, t, x ? x + ((size_t)s * T + t) * H : NULL,
-                                   topk_idx, topk_w, send_pos, recv_base, recv_x, recv_topk_idx,
+                if (dispatch_token(R, T, K, E, sizeof(uint16_t) * (size_t)H, s, t,
+                                   x ? x + ((size_t)s * T + t) * H : NULL, NULL, 0, topk_idx, topk_w,
+                                   send_pos, recv_base, recv_x, NULL, recv_topk_idx, recv_topk_w,
+                                   recv_src_info) != 0)
+                    return -1;
+        }
+    return 0;
+}
+
+/* FP8 dispatch: [RT] intranodeDispatch / internodeDispatch with an element
+ * size of one byte and num_scales fp32 scales per token (x_scales ->
+ * recv_x_scales).  The same placement as oracle_dispatch; each row is H bytes
+ * and its scales row travels with it.  x_scales / recv_x_scales may be NULL
+ * when S == 0, the top-k arrays NULL in cached mode. */
+int oracle_dispatch_fp8(int R, int T, int K, int E, int H, int C, int S,
+                        const uint8_t* x,          /* [R][T][H] */
+                        const float* x_scales,     /* [R][T][S] or NULL */
+                        const int64_t* topk_idx,   /* [R][T][K] or NULL */
+                        const float* topk_w,       /* [R][T][K] or NULL */
+                        const int32_t* send_pos,   /* [R][T][R] */
+                        const int64_t* recv_base,  /* [R+1] */
+                        uint8_t* recv_x,           /* [rows][H] */
+                        float* recv_x_scales,      /* [rows][S] or NULL */
+                        int64_t* recv_topk_idx,    /* [rows][K] or NULL */
+                        float* recv_topk_w,        /* [rows][K] or NULL */
+                        int32_t* recv_src_info)    /* [rows][2] or NULL */
+{
+    for (int s = 0; s < R; ++s)
+        for (int c = 0; c < C; ++c) {
+            int b, e;
+            channel_range(T, C, c, &b, &e);
+            for (int t = b; t < e; ++t)
+                if (dispatch_token(R, T, K, E, (size_t)H, s, t, x + ((size_t)s * T + t) * H,
+                                   x_scales ? x_scales + ((size_t)s * T + t) * S : NULL, S, topk_idx,
+                                   topk_w, send_pos, recv_base, recv_x, recv_x_scales, recv_topk_idx,
                                    recv_topk_w, recv_src_info) != 0)
                     return -1;
         }

@@ -365,9 +365,28 @@ def check_dispatch_cached_mode(o):
         np.testing.assert_array_equal(cached["recv_src_info"], dp["recv_src_info"])
 
 
+def check_dispatch_fp8(o):
+    """FP8 rows and their scales land where the stable sort puts the token."""
+    rng = np.random.default_rng(11)
+    for sh in SHAPES:
+        w, idx, wt, x = make_case(**{**sh, "H": 16})
+        xb = rng.integers(0, 256, size=(w.R, w.T, w.H), dtype=np.uint8)
+        xs = rng.standard_normal((w.R, w.T, 3)).astype(np.float32)
+        lay, nt, dp = run(o, w, idx, wt, x)
+        f8 = o.dispatch_fp8(w.R, w.T, w.K, w.E, w.H, w.C, xb, xs, idx, wt, nt["send_pos"], nt["recv_base"])
+        M = membership(w.R, w.E, idx)
+        s_i, t_i, r_i = np.nonzero(M)
+        perm = np.argsort(r_i, kind="stable")
+        np.testing.assert_array_equal(f8["recv_x"], xb[s_i[perm], t_i[perm]])
+        np.testing.assert_array_equal(f8["recv_x_scales"], xs[s_i[perm], t_i[perm]])
+        np.testing.assert_array_equal(f8["recv_topk_idx"], dp["recv_topk_idx"])
+        np.testing.assert_array_equal(f8["recv_src_info"], dp["recv_src_info"])
+
+
 ALL_CHECKS = [
     check_hand_worked, check_channel_ranges_hand, check_layout_library, check_notify_library,
     check_channel_independence, check_dispatch_stable_sort, check_dispatch_counting_sort,
     check_dispatch_identity_rank, check_dispatch_topk_fields, check_combine_identity_closed_form,
     check_combine_error_bound, check_combine_order, check_bf16_rounding, check_dispatch_cached_mode,
+    check_dispatch_fp8,
 ]

@@ -26,7 +26,7 @@ def ep():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ep_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(ep):
@@ -42,7 +42,7 @@ def declared_arity():
     """Parameter count of every function the header declares."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     out = {}
-    for m in re.finditer(r"\b(ep_[a-z_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+    for m in re.finditer(r"\b(ep_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
         params = m.group(2).strip()
         out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
     return out

@@ -373,3 +373,37 @@ def test_cached_mode_reuses_the_handle(name):
 def gen_x_seeded(w, seed):
     from combine_get_dispatch_notify_gb300.workloads import gen_x
     return gen_x(w.replace(seed=seed))
+
+
+@pytest.mark.parametrize("name", ["tiny", "low_latency", "prefill", "top1_counting_sort", "channels_exceed_tokens"])
+@pytest.mark.parametrize("cached", [False, True], ids=["full", "cached"])
+def test_dispatch_fp8_matches_oracle(name, cached):
+    """FP8 rows (bytes) and their per-token scales go where the bf16 rows go."""
+    w = CONFIGS.get(name) or EDGE[name]
+    o = oracle.load()
+    idx, wt, _ = make_inputs(w)
+    g = torch.Generator().manual_seed(5)
+    S = max(1, w.H // 128)
+    xb = torch.randint(0, 256, (w.R, w.T, w.H), generator=g, dtype=torch.uint8)
+    xs = torch.randn(w.R, w.T, S, generator=g)
+    sh, lay, nt, status = run_layout_notify(w, idx)
+    cap = max(1, worst_case_rows(w))
+    rx = torch.empty(cap, w.H, dtype=torch.uint8, device="cuda")
+    rs = torch.empty(cap, S, dtype=torch.float32, device="cuda")
+    rti = None if cached else torch.empty(cap, w.K, dtype=torch.int64, device="cuda")
+    rtw = None if cached else torch.empty(cap, w.K, dtype=torch.float32, device="cuda")
+    rsi = torch.empty(cap, 2, dtype=torch.int32, device="cuda")
+    ep.ep_dispatch_fp8(sh, xb.cuda(), xs.cuda(), None if cached else idx.cuda(), None if cached else wt.cuda(),
+                       nt["send_pos"], nt["recv_base"], rx, rs, rti, rtw, rsi, status)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+    nt_ref = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref)
+    ref = o.dispatch_fp8(w.R, w.T, w.K, w.E, w.H, w.C, xb.numpy(), xs.numpy(), idx.numpy(), wt.numpy(),
+                         nt_ref["send_pos"], nt_ref["recv_base"], with_topk=not cached)
+    rows = int(nt_ref["recv_base"][-1])
+    assert_equal("recv_x (fp8)", rx[:rows].cpu().numpy(), ref["recv_x"])
+    assert_equal("recv_x_scales", rs[:rows].cpu().numpy(), ref["recv_x_scales"])
+    assert_equal("recv_src_info", rsi[:rows].cpu().numpy(), ref["recv_src_info"])
+    if not cached:
+        assert_equal("recv_topk_idx", rti[:rows].cpu().numpy(), ref["recv_topk_idx"])
+        assert_equal("recv_topk_w", rtw[:rows].cpu().numpy(), ref["recv_topk_w"])
