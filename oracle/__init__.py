@@ -38,7 +38,7 @@ def build(mutant: int = 0) -> str:
     tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
            f"-DORACLE_MUTANT={mutant}", _SRC, "-o", tmp]
-    subprocess.check_call(cmd)
+    subprocess.check_call(cmd + ["-lm"])
     os.replace(tmp, out)
     return out
 
@@ -56,7 +56,8 @@ class Oracle:
     def __init__(self, path: str):
         self.lib = ctypes.CDLL(path)
         for fn in ("oracle_layout", "oracle_notify", "oracle_dispatch", "oracle_dispatch_fp8",
-                   "oracle_combine", "oracle_num_nodes"):
+                   "oracle_combine", "oracle_num_nodes", "oracle_ll_layout", "oracle_ll_dispatch",
+                   "oracle_ll_combine"):
             getattr(self.lib, fn).restype = ctypes.c_int
         self.lib.oracle_f32_to_bf16.restype = None
 
@@ -185,6 +186,42 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_combine: a row lies outside y")
         return dict(combined_x=cx, combined_w=cw)
+
+
+# -- low-latency (per-expert packed) layout -------------------------------------------
+def ll_layout(o: "Oracle", R, T, K, E, cap, topk_idx):
+    """Row of every slot inside its expert's buffer, per-source ranges, counts."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int64).reshape(R, T, K)
+    out = dict(slot_pos=np.zeros((R, T, K), np.int32), layout_range=np.zeros((E, R, 2), np.int32),
+               count=np.zeros((E,), np.int32))
+    rc = o.lib.oracle_ll_layout(R, T, K, E, cap, _p(idx), _p(out["slot_pos"]), _p(out["layout_range"]),
+                                _p(out["count"]))
+    if rc < 0:
+        raise ValueError("oracle_ll_layout: expert id outside [-1, E)")
+    out["dropped"] = rc == 1
+    return out
+
+
+def ll_dispatch(o: "Oracle", R, T, K, E, H, cap, x, topk_idx, slot_pos):
+    recv_x = np.zeros((E, cap, H), np.uint16)
+    src = np.full((E, cap, 2), -1, np.int32)
+    rc = o.lib.oracle_ll_dispatch(R, T, K, E, H, cap, _p(np.ascontiguousarray(x, dtype=np.uint16)),
+                                  _p(np.ascontiguousarray(topk_idx, dtype=np.int64)),
+                                  _p(np.ascontiguousarray(slot_pos, dtype=np.int32)), _p(recv_x), _p(src))
+    if rc != 0:
+        raise ValueError("oracle_ll_dispatch: row outside its buffer")
+    return dict(recv_x=recv_x, recv_src_info=src)
+
+
+def ll_combine(o: "Oracle", R, T, K, E, H, cap, y, topk_idx, topk_w, slot_pos):
+    out = np.zeros((R, T, H), np.uint16)
+    rc = o.lib.oracle_ll_combine(R, T, K, E, H, cap, _p(np.ascontiguousarray(y, dtype=np.uint16)),
+                                 _p(np.ascontiguousarray(topk_idx, dtype=np.int64)),
+                                 _p(np.ascontiguousarray(topk_w, dtype=np.float32)),
+                                 _p(np.ascontiguousarray(slot_pos, dtype=np.int32)), _p(out))
+    if rc != 0:
+        raise ValueError("oracle_ll_combine: row outside its buffer")
+    return out
 
 
 def load(mutant: int = 0) -> Oracle:

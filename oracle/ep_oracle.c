@@ -38,12 +38,13 @@
  */
 #include <stddef.h>
 #include <stdint.h>
+#include <math.h>
 #include <string.h>
 
 #define NODE_SIZE 8 /* ranks per node: NUM_MAX_NVL_PEERS, [AR] 2.2 */
 
 /* Planted mistakes.  The default build (ORACLE_MUTANT 0) has none.  The
- * tests compile copies with ORACLE_MUTANT = 1..8, each carrying one plausible
+ * tests compile copies with ORACLE_MUTANT = 1..10, each carrying one plausible
  * error, and check that the pins reject every one of them. */
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
@@ -404,6 +405,117 @@ int oracle_combine(int R, int T, int K, int H, int64_t y_rows,
                         if (pos[r] >= 0) acc += y_w[(size_t)(recv_base[r] + pos[r]) * K + k];
                     combined_w[((size_t)s * T + t) * K + k] = acc;
                 }
+            }
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Low-latency (per-expert packed) layout.  The pages give only this mode's
+ * transport ([RT] "Intra-node LL fast path setup": peer pointers, fabric IPC,
+ * proxy threads for LL combine); the plain reading used here:
+ *   - every non-masked top-k slot (s,t,k) that names expert e is one row of
+ *     e's receive buffer (a token travels once per expert, not per rank);
+ *   - rows of a buffer are in ascending (source rank, token, slot) order;
+ *   - layout_range[e][s] = (first row, rows) of source s in e's buffer, and
+ *     count[e] = rows in e's buffer;
+ *   - LL combine applies the routing weights: out[s][t] =
+ *     bf16_rne(sum over valid k ascending of fma(w[s][t][k], y[e_k][row_k], acc))
+ *     starting from +0, with the fused multiply-add rounded once per step.
+ * Buffers hold `cap` rows each; a slot whose row would reach cap is dropped
+ * (pos -1).  Returns -1 on an expert id outside [-1, E), 1 when a row was
+ * dropped, else 0. */
+int oracle_ll_layout(int R, int T, int K, int E, int cap,
+                     const int64_t* topk_idx,  /* [R][T][K] */
+                     int32_t* slot_pos,        /* [R][T][K] row inside its expert's buffer, or -1 */
+                     int32_t* layout_range,    /* [E][R][2] */
+                     int32_t* count)           /* [E] */
+{
+    int dropped = 0;
+    memset(count, 0, sizeof(int32_t) * (size_t)E);
+    for (int s = 0; s < R; ++s) {
+        for (int e = 0; e < E; ++e) {
+            layout_range[((size_t)e * R + s) * 2 + 0] = count[e];
+            layout_range[((size_t)e * R + s) * 2 + 1] = 0;
+        }
+        for (int t = 0; t < T; ++t)
+            for (int kk = 0; kk < K; ++kk) {
+                int k = MUT(10) ? K - 1 - kk : kk;
+                size_t at = ((size_t)s * T + t) * K + k;
+                int64_t e = topk_idx[at];
+                if (e < -1 || e >= E) return -1;
+                if (e < 0) {
+                    slot_pos[at] = -1;
+                    continue;
+                }
+                int32_t row = count[e];
+                count[e] += 1;
+                layout_range[((size_t)e * R + s) * 2 + 1] += 1;
+                if (row >= cap) {
+                    slot_pos[at] = -1;
+                    dropped = 1;
+                } else {
+                    slot_pos[at] = row;
+                }
+            }
+    }
+    return dropped;
+}
+
+/* LL dispatch: copy each token row to every (expert, row) its slots name. */
+int oracle_ll_dispatch(int R, int T, int K, int E, int H, int cap,
+                       const uint16_t* x,          /* [R][T][H] */
+                       const int64_t* topk_idx,    /* [R][T][K] */
+                       const int32_t* slot_pos,    /* [R][T][K] */
+                       uint16_t* recv_x,           /* [E][cap][H] */
+                       int32_t* recv_src_info)     /* [E][cap][2] */
+{
+    for (int s = 0; s < R; ++s)
+        for (int t = 0; t < T; ++t)
+            for (int k = 0; k < K; ++k) {
+                size_t at = ((size_t)s * T + t) * K + k;
+                int64_t e = topk_idx[at];
+                int32_t row = slot_pos[at];
+                if (e < 0 || row < 0) continue;
+                if (row >= cap || e >= E) return -1;
+                size_t dst = (size_t)e * cap + row;
+                memcpy(recv_x + dst * H, x + ((size_t)s * T + t) * H, sizeof(uint16_t) * (size_t)H);
+                recv_src_info[dst * 2 + 0] = s;
+                recv_src_info[dst * 2 + 1] = t;
+            }
+    return 0;
+}
+
+/* LL combine: weighted sum over the token's slots, ascending k. */
+int oracle_ll_combine(int R, int T, int K, int E, int H, int cap,
+                      const uint16_t* y,          /* [E][cap][H] */
+                      const int64_t* topk_idx,    /* [R][T][K] */
+                      const float* topk_w,        /* [R][T][K] */
+                      const int32_t* slot_pos,    /* [R][T][K] */
+                      uint16_t* combined_x)       /* [R][T][H] */
+{
+    for (int s = 0; s < R; ++s)
+        for (int t = 0; t < T; ++t) {
+            size_t tok = (size_t)s * T + t;
+            for (int k = 0; k < K; ++k) {
+                int64_t e = topk_idx[tok * K + k];
+                int32_t row = slot_pos[tok * K + k];
+                if (e >= E || row >= cap) return -1;
+            }
+            for (int h = 0; h < H; ++h) {
+                float acc = 0.0f;
+                for (int k = 0; k < K; ++k) {
+                    int64_t e = topk_idx[tok * K + k];
+                    int32_t row = slot_pos[tok * K + k];
+                    if (e < 0 || row < 0) continue;
+                    if (MUT(9)) {
+                        float prod = topk_w[tok * K + k] * bf16_to_f32(y[((size_t)e * cap + row) * H + h]);
+                        acc += prod;
+                    } else {
+                        acc = fmaf(topk_w[tok * K + k], bf16_to_f32(y[((size_t)e * cap + row) * H + h]), acc);
+                    }
+                }
+                combined_x[tok * H + h] = f32_to_bf16(acc);
             }
         }
     return 0;

@@ -19,6 +19,7 @@ import numpy as np
 import torch
 
 from combine_get_dispatch_notify_gb300.workloads import Workload, gen_routing, gen_x
+import oracle as oracle_mod
 from oracle import bf16_bits_to_f32
 
 NODE = 8
@@ -383,10 +384,102 @@ def check_dispatch_fp8(o):
         np.testing.assert_array_equal(f8["recv_src_info"], dp["recv_src_info"])
 
 
+# --------------------------------------------------------------------------- LL packed layout
+def check_ll_layout_library(o):
+    """Row of each slot in its expert's buffer = its rank in a stable sort by expert
+    of the (source, token, slot) sequence; ranges and counts from bincount/cumsum."""
+    for sh in SHAPES:
+        w, idx, wt, x = make_case(**sh)
+        R, T, K, E = w.R, w.T, w.K, w.E
+        cap = R * T * K
+        ll = oracle_mod.ll_layout(o, R, T, K, E, cap, idx)
+        flat = idx.reshape(-1)
+        valid = np.nonzero(flat >= 0)[0]
+        order = valid[np.argsort(flat[valid], kind="stable")]
+        want = np.full(flat.shape, -1, np.int64)
+        keys = flat[order]
+        starts = np.searchsorted(keys, keys, side="left")
+        want[order] = np.arange(len(order)) - starts
+        np.testing.assert_array_equal(ll["slot_pos"].reshape(-1), want)
+        per = np.stack([np.bincount(idx[s_][idx[s_] >= 0], minlength=E) for s_ in range(R)])  # [s, e]
+        np.testing.assert_array_equal(ll["count"], per.sum(0))
+        begin = np.cumsum(per, axis=0) - per
+        np.testing.assert_array_equal(ll["layout_range"][:, :, 0], begin.T)
+        np.testing.assert_array_equal(ll["layout_range"][:, :, 1], per.T)
+        assert not ll["dropped"]
+
+
+def check_ll_dispatch_and_combine(o):
+    """LL dispatch places x rows where the layout says; combine with unit weights
+    is bf16(n * x) (exact fp32 sum); random weights stay within the fp64 bound."""
+    rng = np.random.default_rng(13)
+    for sh in SHAPES:
+        w, idx, wt, x = make_case(**sh)
+        R, T, K, E, H = w.R, w.T, w.K, w.E, w.H
+        cap = R * T * K
+        ll = oracle_mod.ll_layout(o, R, T, K, E, cap, idx)
+        dp = oracle_mod.ll_dispatch(o, R, T, K, E, H, cap, x, idx, ll["slot_pos"])
+        ss, tt, kk = np.nonzero(idx >= 0)
+        ee, rr = idx[ss, tt, kk], ll["slot_pos"][ss, tt, kk]
+        np.testing.assert_array_equal(dp["recv_x"][ee, rr], x[ss, tt])
+        np.testing.assert_array_equal(dp["recv_src_info"][ee, rr], np.stack([ss, tt], 1))
+        assert (dp["recv_src_info"][..., 0] >= 0).sum() == len(ss)  # every slot lands once
+        ones = np.ones_like(wt)
+        cx = oracle_mod.ll_combine(o, R, T, K, E, H, cap, dp["recv_x"], idx, ones, ll["slot_pos"])
+        n = (idx >= 0).sum(-1).astype(np.float32)
+        xf = torch.from_numpy(bf16_bits_to_f32(x))
+        want = (xf * torch.from_numpy(n)[..., None]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        want = np.where(n[..., None] == 0, np.uint16(0), want)
+        np.testing.assert_array_equal(cx, want)
+        y = o.f32_to_bf16(rng.standard_normal((E, cap, H)).astype(np.float32))
+        wr = rng.standard_normal((R, T, K)).astype(np.float32)
+        cx = oracle_mod.ll_combine(o, R, T, K, E, H, cap, y, idx, wr, ll["slot_pos"])
+        yf = bf16_bits_to_f32(y).astype(np.float64)
+        got = bf16_bits_to_f32(cx).astype(np.float64)
+        terms = np.zeros((R, T, K, H))
+        for s_, t_, k_ in zip(ss, tt, kk):
+            terms[s_, t_, k_] = float(wr[s_, t_, k_]) * yf[idx[s_, t_, k_], ll["slot_pos"][s_, t_, k_]]
+        exact = terms.sum(2)
+        bound = 2.0 ** -8 * np.abs(exact) + K * 2.0 ** -23 * np.abs(terms).sum(2) + 1e-30
+        assert (np.abs(got - exact) <= bound).all()
+
+
+def check_ll_combine_order_and_fma(o):
+    """Hand cases, R=1, T=1, E=3 experts, one slot each (cap 1).
+
+    Order: y = 2^24, 1, -2^24 with unit weights in slots 0,1,2 -> (2^24+1)-2^24
+    rounds to 0 in ascending slot order (1 in descending).
+    Fused multiply-add: slot 0 w=-1, y=1+2^-7; slot 1 w=1+2^-23, y=1+2^-7.
+    The exact product of slot 1 is 1+2^-7+2^-23+2^-30; with one rounding per
+    fused step the sum is 2^-23+2^-30 = 2^-23(1+2^-7) (a bf16 value); a
+    separate multiply would drop 2^-30 first and give 2^-23.
+    """
+    idx = np.array([[[0, 1, 2]]], np.int64)
+    ll = oracle_mod.ll_layout(o, 1, 1, 3, 3, 1, idx)
+    y = o.f32_to_bf16(np.array([[[2.0 ** 24]], [[1.0]], [[-(2.0 ** 24)]]], np.float32))
+    cx = oracle_mod.ll_combine(o, 1, 1, 3, 3, 1, 1, y, idx, np.ones((1, 1, 3), np.float32), ll["slot_pos"])
+    assert bf16_bits_to_f32(cx)[0, 0, 0] == 0.0
+    y = o.f32_to_bf16(np.array([[[1 + 2.0 ** -7]], [[1 + 2.0 ** -7]], [[0.0]]], np.float32))
+    wts = np.array([[[-1.0, 1 + 2.0 ** -23, 0.0]]], np.float32)
+    cx = oracle_mod.ll_combine(o, 1, 1, 3, 3, 1, 1, y, idx, wts, ll["slot_pos"])
+    assert bf16_bits_to_f32(cx)[0, 0, 0] == np.float32(2.0 ** -23 * (1 + 2.0 ** -7))
+
+
+def check_ll_capacity_drop(o):
+    """Slots whose row would reach the buffer size are dropped (-1), the rest keep their rows."""
+    w, idx, wt, x = make_case(R=4, T=20, K=3, E=8, H=8, C=2)
+    full = oracle_mod.ll_layout(o, 4, 20, 3, 8, 4 * 20 * 3, idx)
+    small = oracle_mod.ll_layout(o, 4, 20, 3, 8, 5, idx)
+    keep = full["slot_pos"] < 5
+    np.testing.assert_array_equal(small["slot_pos"][keep], full["slot_pos"][keep])
+    assert (small["slot_pos"][~keep] == -1).all() and small["dropped"] == (~keep & (idx >= 0)).any()
+
+
 ALL_CHECKS = [
     check_hand_worked, check_channel_ranges_hand, check_layout_library, check_notify_library,
     check_channel_independence, check_dispatch_stable_sort, check_dispatch_counting_sort,
     check_dispatch_identity_rank, check_dispatch_topk_fields, check_combine_identity_closed_form,
     check_combine_error_bound, check_combine_order, check_bf16_rounding, check_dispatch_cached_mode,
-    check_dispatch_fp8,
+    check_dispatch_fp8, check_ll_layout_library, check_ll_dispatch_and_combine,
+    check_ll_combine_order_and_fma, check_ll_capacity_drop,
 ]

@@ -21,6 +21,8 @@ MUTANTS = {
     6: "received top-k ids left global",
     7: "a token counted once per slot instead of once per rank",
     8: "bf16 conversion truncates instead of rounding",
+    9: "LL combine rounds the product before adding (no fused multiply-add)",
+    10: "LL layout visits a token's slots in descending order",
 }
 
 
