@@ -52,6 +52,9 @@ struct DispatchArgs {
     int64_t* recv_topk_idx;
     float* recv_topk_w;
     int32_t* recv_src_info;
+    const int32_t* ll_slot_pos;  // low-latency layout: [R*T][K] row in the slot's expert buffer, else NULL
+    long long ll_cap;            // rows per expert buffer (low-latency layout)
+    int E;
     const float* x_scales;   // [R*T][num_scales] or NULL (FP8 rows)
     float* recv_x_scales;    // [capacity][num_scales] or NULL
     int num_scales;
@@ -62,6 +65,38 @@ struct DispatchArgs {
     long long num_units;
     long long wait_limit_ns;
 };
+
+// Destination row this lane stands for, or -1: lane r = rank r through
+// send_pos, or in the low-latency layout lane k = top-k slot k, whose row is
+// expert * cap + slot_pos.  Rows outside the receive arrays are refused and
+// reported.
+__device__ __forceinline__ long long lane_row(const DispatchArgs& p, const long long* base, long long g,
+                                              int lane) {
+    if (p.ll_slot_pos != nullptr) {
+        if (lane >= p.K) return -1;
+        const long long e = __ldg(p.topk_idx + g * p.K + lane);
+        const int32_t pos = __ldg(p.ll_slot_pos + g * p.K + lane);
+        if (e < 0 || pos < 0) return -1;
+        if (e >= p.E || pos >= p.ll_cap) {
+            flag_error(p.status, EP_DEV_INCONSISTENT);
+            return -1;
+        }
+        return e * p.ll_cap + pos;
+    }
+    if (lane >= p.R) return -1;
+    const int32_t sp = __ldg(p.send_pos + g * p.R + lane);
+    if (sp < 0) return -1;
+    const long long row = base[lane] + sp;
+    if (row >= p.capacity) {
+        flag_error(p.status, EP_DEV_CAPACITY);
+        return -1;
+    }
+    if (row >= base[lane + 1]) {
+        flag_error(p.status, EP_DEV_INCONSISTENT);
+        return -1;
+    }
+    return row;
+}
 
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -100,7 +135,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         }
     }
     griddep_wait();  // send_pos / recv_base from notify are visible from here on
-    if (tid <= p.R) base[tid] = p.recv_base[tid];
+    if (p.recv_base != nullptr && tid <= p.R) base[tid] = p.recv_base[tid];
     __syncthreads();
 
     if (warp == 0) {
@@ -110,8 +145,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             const long long g = u / p.parts;
             const int part = static_cast<int>(u - g * p.parts);
-            const int32_t sp = lane < p.R ? __ldg(p.send_pos + g * p.R + lane) : -1;
-            const unsigned valid = __ballot_sync(0xffffffffu, sp >= 0);
+            const long long row = lane_row(p, base, g, lane);
+            const unsigned valid = __ballot_sync(0xffffffffu, row >= 0);
             const int slot = k % S;
             const long long off = static_cast<long long>(part) * p.part_bytes;
             const long long left = p.row_bytes - off;
@@ -130,17 +165,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                              bytes, &full[slot]);
                 }
             }
-            if (sp >= 0) {
-                long long row = base[lane] + sp;
-                if (row >= p.capacity) {
-                    flag_error(p.status, EP_DEV_CAPACITY);
-                    row = -1;
-                } else if (row >= base[lane + 1]) {
-                    flag_error(p.status, EP_DEV_INCONSISTENT);
-                    row = -1;
-                }
-                desc[slot].rows[__popc(valid & lanemask_lt())] = row;
-            }
+            if (row >= 0) desc[slot].rows[__popc(valid & lanemask_lt())] = row;
             if (lane == 0) {
                 desc[slot].n = __popc(valid);
                 desc[slot].bytes = bytes;
@@ -220,7 +245,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
             if ((i++ & 1) != mw) continue;
             const long long g = u / p.parts;
             const int s = static_cast<int>(g / p.T), t = static_cast<int>(g - static_cast<long long>(s) * p.T);
-            const int32_t sp = lane < p.R ? __ldg(p.send_pos + g * p.R + lane) : -1;
+            const long long my_row = lane_row(p, base, g, lane);
             long long e = -1;
             float w = 0.0f;
             int owner = -1;
@@ -229,12 +254,11 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                 w = __ldg(p.topk_w + g * p.K + lane);
                 owner = e >= 0 ? static_cast<int>(e / p.E_loc) : -1;
             }
-            unsigned m = __ballot_sync(0xffffffffu, sp >= 0);
+            unsigned m = __ballot_sync(0xffffffffu, my_row >= 0);
             while (m) {
-                const int r = __ffs(m) - 1;
+                const int r = __ffs(m) - 1;  // rank r (or, low-latency layout, slot r)
                 m &= m - 1;
-                const long long row = base[r] + __shfl_sync(0xffffffffu, sp, r);
-                if (row >= p.capacity || row >= base[r + 1]) continue;
+                const long long row = __shfl_sync(0xffffffffu, my_row, r);
                 if (with_topk && lane < p.K) {
                     const bool here = owner == r;
                     p.recv_topk_idx[row * p.K + lane] = here ? e - static_cast<long long>(r) * p.E_loc : -1;
@@ -251,19 +275,14 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 
 }  // namespace
 
-cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, const float* x_scales,
-                            int num_scales, const int64_t* topk_idx, const float* topk_w,
-                            const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
-                            void* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
-                            float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                            cudaStream_t stream) {
-    const long long tokens = static_cast<long long>(sh.R) * sh.T;
-    if (tokens == 0) return cudaSuccess;
+namespace {
+
+// Sizes the ring for the row bytes in `p` and launches.
+cudaError_t launch_dispatch_args(DispatchArgs& p, long long tokens, cudaStream_t stream) {
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const long long grid_target = static_cast<long long>(sms) * kCtasPerSm;
-    const long long row_bytes = static_cast<long long>(sh.H) * x_elem_bytes;
-
+    const long long row_bytes = p.row_bytes;
     // Row parts: at most 32 KB, and split further (down to 2 KB) while there
     // are fewer than 8 units per CTA.  Parts are multiples of 16 bytes.
     long long part = row_bytes < kMaxPartBytes ? row_bytes : kMaxPartBytes;
@@ -272,8 +291,40 @@ cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, co
     const int parts = static_cast<int>((row_bytes + part - 1) / part);
     int slots = static_cast<int>(kSmemBudget / part);
     slots = slots < 2 ? 2 : (slots > kMaxSlots ? kMaxSlots : slots);
+    p.parts = parts;
+    p.slots = slots;
+    p.part_bytes = static_cast<uint32_t>(part);
+    p.num_units = tokens * parts;
+    p.wait_limit_ns = kDefaultWaitLimitNs;
+    const size_t smem = static_cast<size_t>(slots) * part + 2 * slots * sizeof(uint64_t) +
+                        slots * sizeof(SlotDesc) + 33 * sizeof(long long);
+    const long long grid = p.num_units < grid_target ? p.num_units : grid_target;
+    return launch_pdl(dispatch_kernel, dim3(static_cast<unsigned>(grid)), dim3(kDispatchThreads), smem,
+                      stream, 0, true, p);
+}
 
-    DispatchArgs p;
+DispatchArgs base_args(const Shape& sh, int32_t* status) {
+    DispatchArgs p = {};
+    p.status = status;
+    p.R = sh.R;
+    p.T = sh.T;
+    p.K = sh.K;
+    p.E = sh.E;
+    p.E_loc = sh.E_loc;
+    return p;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, const float* x_scales,
+                            int num_scales, const int64_t* topk_idx, const float* topk_w,
+                            const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
+                            void* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
+                            float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                            cudaStream_t stream) {
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (tokens == 0) return cudaSuccess;
+    DispatchArgs p = base_args(sh, status);
     p.x = static_cast<const uint8_t*>(x);
     p.x_scales = x_scales;
     p.recv_x_scales = recv_x_scales;
@@ -287,23 +338,25 @@ cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, co
     p.recv_topk_idx = recv_topk_idx;
     p.recv_topk_w = recv_topk_w;
     p.recv_src_info = recv_src_info;
-    p.status = status;
-    p.R = sh.R;
-    p.T = sh.T;
-    p.K = sh.K;
-    p.E_loc = sh.E_loc;
-    p.parts = parts;
-    p.slots = slots;
-    p.part_bytes = static_cast<uint32_t>(part);
-    p.row_bytes = row_bytes;
-    p.num_units = tokens * parts;
-    p.wait_limit_ns = kDefaultWaitLimitNs;
+    p.row_bytes = static_cast<long long>(sh.H) * x_elem_bytes;
+    return launch_dispatch_args(p, tokens, stream);
+}
 
-    const size_t smem = static_cast<size_t>(slots) * part + 2 * slots * sizeof(uint64_t) +
-                        slots * sizeof(SlotDesc) + 33 * sizeof(long long);
-    const long long grid = p.num_units < grid_target ? p.num_units : grid_target;
-    return launch_pdl(dispatch_kernel, dim3(static_cast<unsigned>(grid)), dim3(kDispatchThreads), smem,
-                      stream, 0, true, p);
+cudaError_t launch_ll_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
+                               const int32_t* slot_pos, int cap, uint16_t* recv_x,
+                               int32_t* recv_src_info, int32_t* status, cudaStream_t stream) {
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (tokens == 0) return cudaSuccess;
+    DispatchArgs p = base_args(sh, status);
+    p.x = reinterpret_cast<const uint8_t*>(x);
+    p.topk_idx = topk_idx;
+    p.ll_slot_pos = slot_pos;
+    p.ll_cap = cap;
+    p.capacity = static_cast<long long>(sh.E) * cap;
+    p.recv_x = reinterpret_cast<uint8_t*>(recv_x);
+    p.recv_src_info = recv_src_info;
+    p.row_bytes = sh.row_bytes();
+    return launch_dispatch_args(p, tokens, stream);
 }
 
 }  // namespace ep

@@ -296,6 +296,51 @@ ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* 
                                             combined_w, status, stream));
 }
 
+ep_status_t ep_ll_layout(const ep_shape_t* shape, const int64_t* topk_idx,
+                         const int32_t* num_tokens_per_expert, int32_t expert_capacity,
+                         int32_t* slot_pos, int32_t* layout_range, int32_t* count, int32_t* status,
+                         cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh) || expert_capacity < 0) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (!ep::array_ok(topk_idx, tokens * sh.K, 8) || !ep::aligned4(num_tokens_per_expert) ||
+        !ep::array_ok(slot_pos, tokens * sh.K, 4) || !ep::aligned4(layout_range) || !ep::aligned4(count) ||
+        !ep::aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    return ep::from_cuda(ep::launch_ll_layout(sh, topk_idx, num_tokens_per_expert, expert_capacity, slot_pos,
+                                              layout_range, count, status, stream));
+}
+
+ep_status_t ep_ll_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
+                           const int32_t* slot_pos, int32_t expert_capacity, uint16_t* recv_x,
+                           int32_t* recv_src_info, int32_t* status, cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh) || expert_capacity < 0) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    const long long rows = static_cast<long long>(sh.E) * expert_capacity;
+    if (!ep::array_ok(x, tokens * sh.H, 16) || !ep::array_ok(topk_idx, tokens * sh.K, 8) ||
+        !ep::array_ok(slot_pos, tokens * sh.K, 4) || !ep::array_ok(recv_x, rows * sh.H, 16) ||
+        (recv_src_info != nullptr && !ep::aligned8(recv_src_info)) || !ep::aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    return ep::from_cuda(ep::launch_ll_dispatch(sh, x, topk_idx, slot_pos, expert_capacity, recv_x,
+                                                recv_src_info, status, stream));
+}
+
+ep_status_t ep_ll_combine(const ep_shape_t* shape, const uint16_t* y, int32_t expert_capacity,
+                          const int64_t* topk_idx, const float* topk_w, const int32_t* slot_pos,
+                          uint16_t* combined_x, int32_t* status, cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh) || expert_capacity < 0) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    const long long rows = static_cast<long long>(sh.E) * expert_capacity;
+    if (!ep::array_ok(y, rows * sh.H, 16) || !ep::array_ok(topk_idx, tokens * sh.K, 8) ||
+        !ep::array_ok(topk_w, tokens * sh.K, 4) || !ep::array_ok(slot_pos, tokens * sh.K, 4) ||
+        !ep::array_ok(combined_x, tokens * sh.H, 16) || !ep::aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    return ep::from_cuda(ep::launch_ll_combine(sh, y, expert_capacity, topk_idx, topk_w, slot_pos, combined_x,
+                                               status, stream));
+}
+
 ep_status_t ep_sync_status(const int32_t* status, cudaStream_t stream) {
     if (!ep::aligned4(status)) return EP_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return EP_ERR_CUDA;

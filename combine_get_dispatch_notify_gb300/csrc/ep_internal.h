@@ -72,4 +72,20 @@ cudaError_t launch_combine(const Shape& sh, const uint16_t* y, const float* y_w,
                            const int32_t* send_pos, const int64_t* recv_base, uint16_t* combined_x,
                            float* combined_w, int32_t* status, cudaStream_t stream);
 
+// Low-latency (per-expert packed) layout: row of every top-k slot in its
+// expert's buffer of `cap` rows (-1 when masked or beyond cap), per-source
+// ranges [E][R][2] and per-expert counts [E].
+cudaError_t launch_ll_layout(const Shape& sh, const int64_t* topk_idx, const int32_t* num_tokens_per_expert,
+                             int cap, int32_t* slot_pos, int32_t* layout_range, int32_t* count,
+                             int32_t* status, cudaStream_t stream);
+
+// LL dispatch / combine share the dispatch and combine kernels; rows are
+// resolved from (topk_idx, slot_pos) as expert * cap + pos.
+cudaError_t launch_ll_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
+                               const int32_t* slot_pos, int cap, uint16_t* recv_x,
+                               int32_t* recv_src_info, int32_t* status, cudaStream_t stream);
+cudaError_t launch_ll_combine(const Shape& sh, const uint16_t* y, int cap, const int64_t* topk_idx,
+                              const float* topk_w, const int32_t* slot_pos, uint16_t* combined_x,
+                              int32_t* status, cudaStream_t stream);
+
 }  // namespace ep

@@ -76,6 +76,9 @@ _SIGS = {
                         [_vp] * 6 + [_vp]),
     "ep_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i64] + [_vp] * 5 + [_vp]),
     "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 15 + [_vp, _vp, _vp]),
+    "ep_ll_layout": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "ep_ll_dispatch": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "ep_ll_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ep_sync_status": (_i32, [_vp, _vp]),
     "ep_debug_notify_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 +
                                        [_sz, _vp, _i32, _i32, _vp]),
@@ -314,6 +317,43 @@ def ep_combine(shape: EpShape, y, y_w, send_pos, recv_base, combined_x, combined
         _t(combined_w, torch.float32, (R, T, K), "combined_w", nullable=True),
         _t(status, torch.int32, (1,), "status"), _stream(stream))
     _check("ep_combine", rc)
+
+
+def ep_ll_layout(shape: EpShape, topk_idx, num_tokens_per_expert, expert_capacity: int, slot_pos,
+                 layout_range, count, status, stream=None) -> None:
+    """Low-latency (per-expert packed) layout: row of each slot in its expert's buffer."""
+    R, T, K, E = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.num_experts
+    rc = lib().ep_ll_layout(
+        ctypes.byref(shape), _t(topk_idx, torch.int64, (R, T, K), "topk_idx"),
+        _t(num_tokens_per_expert, torch.int32, (R, E), "num_tokens_per_expert"), _i32(expert_capacity),
+        _t(slot_pos, torch.int32, (R, T, K), "slot_pos"), _t(layout_range, torch.int32, (E, R, 2), "layout_range"),
+        _t(count, torch.int32, (E,), "count"), _t(status, torch.int32, (1,), "status"), _stream(stream))
+    _check("ep_ll_layout", rc)
+
+
+def ep_ll_dispatch(shape: EpShape, x, topk_idx, slot_pos, expert_capacity: int, recv_x, recv_src_info,
+                   status, stream=None) -> None:
+    R, T, K, E, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.num_experts, shape.hidden
+    cap = expert_capacity
+    rc = lib().ep_ll_dispatch(
+        ctypes.byref(shape), _t(x, torch.bfloat16, (R, T, H), "x"),
+        _t(topk_idx, torch.int64, (R, T, K), "topk_idx"), _t(slot_pos, torch.int32, (R, T, K), "slot_pos"),
+        _i32(cap), _t(recv_x, torch.bfloat16, (E, cap, H), "recv_x"),
+        _t(recv_src_info, torch.int32, (E, cap, 2), "recv_src_info", nullable=True),
+        _t(status, torch.int32, (1,), "status"), _stream(stream))
+    _check("ep_ll_dispatch", rc)
+
+
+def ep_ll_combine(shape: EpShape, y, expert_capacity: int, topk_idx, topk_w, slot_pos, combined_x, status,
+                  stream=None) -> None:
+    R, T, K, E, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.num_experts, shape.hidden
+    cap = expert_capacity
+    rc = lib().ep_ll_combine(
+        ctypes.byref(shape), _t(y, torch.bfloat16, (E, cap, H), "y"), _i32(cap),
+        _t(topk_idx, torch.int64, (R, T, K), "topk_idx"), _t(topk_w, torch.float32, (R, T, K), "topk_w"),
+        _t(slot_pos, torch.int32, (R, T, K), "slot_pos"), _t(combined_x, torch.bfloat16, (R, T, H), "combined_x"),
+        _t(status, torch.int32, (1,), "status"), _stream(stream))
+    _check("ep_ll_combine", rc)
 
 
 def ep_sync_status(status, stream=None) -> int:

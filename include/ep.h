@@ -326,6 +326,53 @@ ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* 
                        cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Low-latency layout (per-expert packed).  The pages name this second mode
+ * and give only its transport ([RT] "Intra-node LL fast path setup": peer
+ * pointers for LL dispatch/combine; LL combine's proxy threads); its data
+ * layout here is a plain reading:
+ *   - every non-masked top-k slot (s,t,k) naming expert e is one row of e's
+ *     receive buffer: a token travels once per expert, not once per rank;
+ *   - a buffer holds expert_capacity rows (R*T suffices when a token never
+ *     names an expert twice); rows are in ascending (source rank, token,
+ *     slot) order; a slot whose row would reach the capacity is dropped and
+ *     EP_DEV_CAPACITY is set;
+ *   - combine applies the routing weights (LL combine takes the top-k
+ *     weights): combined_x[s][t] = bf16_rne(acc), acc = +0 and then, for each
+ *     valid slot k ascending, acc = fma(topk_w[s][t][k], y[e_k][row_k], acc)
+ *     (one rounding per step).
+ * Buffers are indexed by global expert e = r*E_loc + j, so [E][cap] is the
+ * same memory as [R][E_loc][cap] ([E_loc, R*T, H] per rank).
+ *
+ * ep_ll_layout
+ *   topk_idx               in  int64 [R][T][K]
+ *   num_tokens_per_expert  in  int32 [R][E]  (from ep_get_dispatch_layout)
+ *   expert_capacity        rows per expert buffer (>= 0)
+ *   slot_pos               out int32 [R][T][K]  row in the slot's expert
+ *                                                buffer, or -1
+ *   layout_range           out int32 [E][R][2]  (first row, rows) of each
+ *                                                source rank in the buffer
+ *   count                  out int32 [E]        rows in each buffer (before
+ *                                                any capacity drop)
+ * ep_ll_dispatch
+ *   x [R][T][H] bf16, topk_idx, slot_pos (from ep_ll_layout) ->
+ *   recv_x [E][expert_capacity][H] bf16, recv_src_info [E][expert_capacity][2]
+ *   (source rank, token; may be NULL).  Rows not written are left as they are.
+ * ep_ll_combine
+ *   y [E][expert_capacity][H] bf16 (expert outputs, recv_x for an identity
+ *   expert), topk_idx, topk_w [R][T][K] fp32, slot_pos -> combined_x [R][T][H].
+ */
+ep_status_t ep_ll_layout(const ep_shape_t* shape, const int64_t* topk_idx,
+                         const int32_t* num_tokens_per_expert, int32_t expert_capacity,
+                         int32_t* slot_pos, int32_t* layout_range, int32_t* count, int32_t* status,
+                         cudaStream_t stream);
+ep_status_t ep_ll_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
+                           const int32_t* slot_pos, int32_t expert_capacity, uint16_t* recv_x,
+                           int32_t* recv_src_info, int32_t* status, cudaStream_t stream);
+ep_status_t ep_ll_combine(const ep_shape_t* shape, const uint16_t* y, int32_t expert_capacity,
+                          const int64_t* topk_idx, const float* topk_w, const int32_t* slot_pos,
+                          uint16_t* combined_x, int32_t* status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Waits for `stream`, reads the device status word (a 4-byte copy into host
  * memory owned by this call), and maps its bits to a status: EP_OK,
  * EP_ERR_TIMEOUT, EP_ERR_CAPACITY, EP_ERR_INPUT or EP_ERR_INCONSISTENT (in

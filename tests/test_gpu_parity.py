@@ -407,3 +407,94 @@ def test_dispatch_fp8_matches_oracle(name, cached):
     if not cached:
         assert_equal("recv_topk_idx", rti[:rows].cpu().numpy(), ref["recv_topk_idx"])
         assert_equal("recv_topk_w", rtw[:rows].cpu().numpy(), ref["recv_topk_w"])
+
+
+# ---------------------------------------------------------------------------- low-latency layout
+LL_CASES = {
+    "tiny": (CONFIGS["tiny"], 1),
+    "low_latency": (CONFIGS["low_latency"], 1),
+    "top1_counting_sort": (EDGE["top1_counting_sort"], 1),
+    "r32_min_hidden_repeats": (EDGE["r32_min_hidden_repeats"], None),  # repeated experts: cap R*T*K
+    "all_masked": (EDGE["all_masked"], 1),
+    "odd_ranks_align": (EDGE["odd_ranks_align"], 1),
+}
+
+
+def _ll_run(w, cap, idx, wt, x, y=None):
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay = ep.alloc_layout(sh)
+    ep.ep_get_dispatch_layout(sh, idx.cuda(), lay["num_tokens_per_rank"], lay["num_tokens_per_rdma_rank"],
+                              lay["num_tokens_per_expert"], lay["is_token_in_rank"], status)
+    slot = torch.empty(w.R, w.T, w.K, dtype=torch.int32, device="cuda")
+    rng_ = torch.empty(w.E, w.R, 2, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(w.E, dtype=torch.int32, device="cuda")
+    ep.ep_ll_layout(sh, idx.cuda(), lay["num_tokens_per_expert"], cap, slot, rng_, cnt, status)
+    rx = torch.zeros(w.E, cap, w.H, dtype=torch.bfloat16, device="cuda")
+    src = torch.full((w.E, cap, 2), -1, dtype=torch.int32, device="cuda")
+    ep.ep_ll_dispatch(sh, x, idx.cuda(), slot, cap, rx, src, status)
+    out = torch.empty(w.R, w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    ep.ep_ll_combine(sh, rx if y is None else y, cap, idx.cuda(), wt.cuda(), slot, out, status)
+    return status, slot, rng_, cnt, rx, src, out
+
+
+@pytest.mark.parametrize("name", sorted(LL_CASES))
+def test_ll_layout_dispatch_combine(name):
+    w, capf = LL_CASES[name]
+    cap = w.R * w.T * (capf or w.K)
+    o = oracle.load()
+    idx, wt, x = make_inputs(w)
+    status, slot, rng_, cnt, rx, src, out = _ll_run(w, cap, idx, wt, x.cuda())
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    ref = oracle.ll_layout(o, w.R, w.T, w.K, w.E, cap, idx.numpy())
+    assert_equal("ll slot_pos", slot.cpu().numpy(), ref["slot_pos"])
+    assert_equal("ll layout_range", rng_.cpu().numpy(), ref["layout_range"])
+    assert_equal("ll count", cnt.cpu().numpy(), ref["count"])
+    # every slot's row holds its token and source info (all slots, any size)
+    s_i, t_i, k_i = np.nonzero(idx.numpy() >= 0)
+    e_i = idx.numpy()[s_i, t_i, k_i]
+    p_i = ref["slot_pos"][s_i, t_i, k_i]
+    if len(s_i):
+        ei, pi = torch.from_numpy(e_i).cuda(), torch.from_numpy(p_i.astype(np.int64)).cuda()
+        got = rx[ei, pi].view(torch.int16)
+        want = x.cuda().view(torch.int16)[torch.from_numpy(s_i).cuda(), torch.from_numpy(t_i).cuda()]
+        assert torch.equal(got, want), "ll recv_x rows differ from their tokens"
+        assert_equal("ll recv_src_info", src[ei, pi].cpu().numpy(), np.stack([s_i, t_i], 1).astype(np.int32))
+    assert int((src[..., 0] >= 0).sum()) == len(s_i)  # nothing else written
+    # combine: oracle on the whole problem when it is small, else on sampled tokens
+    rows_bytes = w.E * cap * w.H * 2
+    if rows_bytes <= (1 << 30):
+        refc = oracle.ll_combine(o, w.R, w.T, w.K, w.E, w.H, cap, u16(rx), idx.numpy(), wt.numpy(),
+                                 ref["slot_pos"])
+        assert_combine_close("ll combined_x", u16(out), refc)
+    else:
+        toks = _sample_tokens(w.R, w.T, 256, 3)
+        ti = idx.numpy().reshape(-1, w.K)[toks]
+        sp = ref["slot_pos"].reshape(-1, w.K)[toks]
+        n = len(toks)
+        # sub-problem: one expert buffer holding row i*K + k for sampled token i, slot k
+        rows = torch.zeros(n * w.K, w.H, dtype=torch.bfloat16, device="cuda")
+        for i in range(n):
+            for k in range(w.K):
+                if ti[i, k] >= 0:
+                    rows[i * w.K + k] = rx[int(ti[i, k]), int(sp[i, k])]
+        sub_idx = np.where(ti >= 0, 0, -1).astype(np.int64).reshape(1, n, w.K)
+        sub_pos = np.where(ti >= 0, np.arange(n * w.K).reshape(n, w.K), -1).astype(np.int32).reshape(1, n, w.K)
+        refc = oracle.ll_combine(o, 1, n, w.K, 1, w.H, n * w.K, u16(rows), sub_idx,
+                                 wt.numpy().reshape(-1, w.K)[toks].reshape(1, n, w.K), sub_pos)
+        got = out.view(-1, w.H)[torch.from_numpy(toks).cuda()]
+        assert_combine_close("ll combined_x (sampled)", u16(got), refc[0])
+
+
+def test_ll_capacity_drop_reports_status():
+    w = CONFIGS["tiny"]
+    cap = 7  # far fewer rows than slots per expert
+    o = oracle.load()
+    idx, wt, x = make_inputs(w)
+    status, slot, rng_, cnt, rx, src, out = _ll_run(w, cap, idx, wt, x.cuda())
+    assert ep.ep_sync_status(status) == ep.EP_ERR_CAPACITY
+    ref = oracle.ll_layout(o, w.R, w.T, w.K, w.E, cap, idx.numpy())
+    assert ref["dropped"]
+    assert_equal("ll slot_pos (capacity)", slot.cpu().numpy(), ref["slot_pos"])
+    refc = oracle.ll_combine(o, w.R, w.T, w.K, w.E, w.H, cap, u16(rx), idx.numpy(), wt.numpy(), ref["slot_pos"])
+    assert_combine_close("ll combined_x (capacity)", u16(out), refc)
