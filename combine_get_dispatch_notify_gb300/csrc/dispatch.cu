@@ -254,6 +254,15 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                 w = __ldg(p.topk_w + g * p.K + lane);
                 owner = e >= 0 ? static_cast<int>(e / p.E_loc) : -1;
             }
+            // the token's FP8 scales, loaded once (lane j holds scales j, j+32, ...)
+            constexpr int kScaleRegs = 4;
+            const bool scales_in_regs = with_scales && p.num_scales <= kScaleRegs * kWarp;
+            float sc[kScaleRegs];
+#pragma unroll
+            for (int c = 0; c < kScaleRegs; ++c) {
+                const int j = lane + c * kWarp;
+                sc[c] = (scales_in_regs && j < p.num_scales) ? __ldg(p.x_scales + g * p.num_scales + j) : 0.0f;
+            }
             unsigned m = __ballot_sync(0xffffffffu, my_row >= 0);
             while (m) {
                 const int r = __ffs(m) - 1;  // rank r (or, low-latency layout, slot r)
@@ -265,9 +274,16 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                     p.recv_topk_w[row * p.K + lane] = here ? w : 0.0f;
                 }
                 if (with_src && lane == 0) *reinterpret_cast<int2*>(p.recv_src_info + row * 2) = make_int2(s, t);
-                if (with_scales)  // the token's FP8 block scales travel with its row
+                if (scales_in_regs) {  // the token's FP8 block scales travel with its row
+#pragma unroll
+                    for (int c = 0; c < kScaleRegs; ++c) {
+                        const int j = lane + c * kWarp;
+                        if (j < p.num_scales) p.recv_x_scales[row * p.num_scales + j] = sc[c];
+                    }
+                } else if (with_scales) {
                     for (int j = lane; j < p.num_scales; j += kWarp)
                         p.recv_x_scales[row * p.num_scales + j] = __ldg(p.x_scales + g * p.num_scales + j);
+                }
             }
         }
     }

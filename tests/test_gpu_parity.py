@@ -498,3 +498,56 @@ def test_ll_capacity_drop_reports_status():
     assert_equal("ll slot_pos (capacity)", slot.cpu().numpy(), ref["slot_pos"])
     refc = oracle.ll_combine(o, w.R, w.T, w.K, w.E, w.H, cap, u16(rx), idx.numpy(), wt.numpy(), ref["slot_pos"])
     assert_combine_close("ll combined_x (capacity)", u16(out), refc)
+
+
+def _random_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        R = int(rng.choice([1, 2, 3, 5, 7, 8, 16, 24, 32]))
+        E_loc = int(rng.integers(1, 9))
+        E = R * E_loc
+        K = int(rng.integers(1, min(8, E) + 1))
+        routing = str(rng.choice(["uniform", "zipf", "replace"]))
+        if routing != "replace" and K > E:
+            K = E
+        out.append(Workload(f"rand{i}", R=R, T=int(rng.integers(0, 300)), H=int(rng.choice([8, 16, 64, 264, 520])),
+                            E=E, K=K, C=int(rng.integers(1, 41)), routing=routing,
+                            mask=float(rng.choice([0.0, 0.2])), seed=int(rng.integers(0, 1000)),
+                            expert_alignment=int(rng.choice([1, 2, 8]))))
+    return out
+
+
+@pytest.mark.parametrize("w", _random_shapes(24, 2024), ids=lambda w: f"{w.name}-R{w.R}T{w.T}K{w.K}E{w.E}H{w.H}C{w.C}")
+def test_random_shapes_all_paths(w):
+    """Seeded random shapes: bf16 path, low-latency layout and FP8 rows against the oracle."""
+    full_parity(w, random_expert=True)
+    cap = w.R * w.T * (w.K if w.routing == "replace" else 1)  # repeated experts need room per slot
+    o = oracle.load()
+    idx, wt, x = make_inputs(w)
+    status, slot, rng_, cnt, rx, src, out = _ll_run(w, max(cap, 1), idx, wt, x.cuda())
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    ref = oracle.ll_layout(o, w.R, w.T, w.K, w.E, max(cap, 1), idx.numpy())
+    assert_equal("ll slot_pos", slot.cpu().numpy(), ref["slot_pos"])
+    assert_equal("ll layout_range", rng_.cpu().numpy(), ref["layout_range"])
+    refc = oracle.ll_combine(o, w.R, w.T, w.K, w.E, w.H, max(cap, 1), u16(rx), idx.numpy(), wt.numpy(),
+                             ref["slot_pos"])
+    assert_combine_close("ll combined_x", u16(out), refc)
+    if w.H % 16 == 0:
+        sh, lay, nt, status = run_layout_notify(w, idx)
+        g = torch.Generator().manual_seed(w.seed)
+        xb = torch.randint(0, 256, (w.R, w.T, w.H), generator=g, dtype=torch.uint8)
+        xs = torch.randn(w.R, w.T, 3, generator=g)
+        capr = max(1, worst_case_rows(w))
+        r8 = torch.empty(capr, w.H, dtype=torch.uint8, device="cuda")
+        rs = torch.empty(capr, 3, dtype=torch.float32, device="cuda")
+        ep.ep_dispatch_fp8(sh, xb.cuda(), xs.cuda(), None, None, nt["send_pos"], nt["recv_base"], r8, rs,
+                           None, None, None, status)
+        assert ep.ep_sync_status(status) == ep.EP_OK
+        lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+        nt_ref = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref)
+        d8 = o.dispatch_fp8(w.R, w.T, w.K, w.E, w.H, w.C, xb.numpy(), xs.numpy(), idx.numpy(), wt.numpy(),
+                            nt_ref["send_pos"], nt_ref["recv_base"], with_topk=False)
+        rows = int(nt_ref["recv_base"][-1])
+        assert_equal("fp8 recv_x", r8[:rows].cpu().numpy(), d8["recv_x"])
+        assert_equal("fp8 recv_x_scales", rs[:rows].cpu().numpy(), d8["recv_x_scales"])
