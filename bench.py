@@ -1,5 +1,5 @@
-"""Benchmark: one step = layout -> notify -> dispatch -> combine (identity
-expert) over one batch of a synthetic workload, through the C ABI.
+"""Benchmark: one step = layout + notify (one call) -> dispatch -> combine
+(identity expert) over one batch of a synthetic workload, through the C ABI.
 
 Prints ONE JSON line (rank 0).  Default workload: the low-latency shape
 (R=16 logical ranks, T=128 tokens/rank, H=7168, top-8 of 256 experts, C=8),
@@ -56,6 +56,8 @@ def algorithmic_bytes(w, P: int) -> dict:
 
     layout   R*T*8K  (top-k ids)          + R*T*R   (is_token_in_rank)
     notify   R*T*R   (is_token_in_rank)   + R*T*R*4 (row map)
+    layout_notify (one call) R*T*8K + R*T*R + R*T*R*4: the membership rows
+             are written once and not read back
     dispatch R*T*(2H + 12K) (x, ids, weights) + P*(2H + 12K + 8) (rows, ids,
              weights, source info)
     combine  P*(2H + 4K + 4) (rows, weights, row map) + R*T*(2H + 4K)
@@ -65,9 +67,15 @@ def algorithmic_bytes(w, P: int) -> dict:
     return {
         "layout": tok * 8 * K + tok * R,
         "notify": tok * R + tok * R * 4,
+        "layout_notify": tok * 8 * K + tok * R + tok * R * 4,
         "dispatch": tok * (2 * H + 12 * K) + P * (2 * H + 12 * K + 8),
         "combine": P * (2 * H + 4 * K + 4) + tok * (2 * H + 4 * K),
     }
+
+
+def step_bytes_of(nb: dict) -> int:
+    """Algorithmic bytes of one whole step: layout + notify as one call, dispatch, combine."""
+    return nb["layout_notify"] + nb["dispatch"] + nb["combine"]
 
 
 def measured_peak():
@@ -231,7 +239,7 @@ def run_reference(args, w):
         if time.perf_counter() - t_all > budget * 4:
             break
     step_s = statistics.mean(sec)
-    b = sum(algorithmic_bytes(w, P).values())
+    b = step_bytes_of(algorithmic_bytes(w, P))
     value = b / step_s / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
@@ -254,7 +262,9 @@ def config_dict(w):
 
 # ----------------------------------------------------------------------------- our arm
 class Step:
-    """The four C-ABI calls with arguments marshalled once (ctypes, device pointers)."""
+    """The C-ABI calls of one step with arguments marshalled once (ctypes, device
+    pointers): ep_layout_notify, ep_dispatch, ep_combine; the separate layout and
+    notify calls are kept for the per-op comparison."""
 
     def __init__(self, ep, pipe, x, idx, wt, stream):
         import ctypes
@@ -273,6 +283,11 @@ class Step:
                             p(La["num_tokens_per_rdma_rank"]), p(La["num_tokens_per_expert"]),
                             *[p(Nt[k]) for k in ep._NOTIFY_OUT], p(Nt["workspace"]),
                             ep._sz(Nt["workspace"].numel()), st, v(None), s)
+        self.layout_notify_args = (self.sh, p(idx), p(La["num_tokens_per_rank"]),
+                                   p(La["num_tokens_per_rdma_rank"]), p(La["num_tokens_per_expert"]),
+                                   p(La["is_token_in_rank"]), *[p(Nt[k]) for k in ep._NOTIFY_OUT],
+                                   p(Nt["workspace"]), ep._sz(Nt["workspace"].numel()), st, v(None), s)
+        self.fused = ep.ep_layout_notify_fused(sh) == 1
         cap = D["recv_x"].shape[0]
         self.dispatch_args = (self.sh, p(x), p(idx), p(wt), p(Nt["send_pos"]), p(Nt["recv_base"]),
                               ep._i64(cap), p(D["recv_x"]), p(D["recv_topk_idx"]), p(D["recv_topk_w"]),
@@ -294,6 +309,10 @@ class Step:
         rc = self.L.ep_notify_dispatch(*self.notify_args)
         assert rc == 0, rc
 
+    def layout_notify(self):
+        rc = self.L.ep_layout_notify(*self.layout_notify_args)
+        assert rc == 0, rc
+
     def dispatch(self):
         rc = self.L.ep_dispatch(*self.dispatch_args)
         assert rc == 0, rc
@@ -303,8 +322,7 @@ class Step:
         assert rc == 0, rc
 
     def all(self):
-        self.layout()
-        self.notify()
+        self.layout_notify()
         self.dispatch()
         self.combine()
 
@@ -338,7 +356,7 @@ def run_ours(args, w):
         assert ep.ep_sync_status(pipe.status, stream) == ep.EP_OK, "device status not OK"
         P = int(pipe.notify["recv_base"][-1].item())
         nbytes = algorithmic_bytes(w, P)
-        step_bytes = sum(nbytes.values())
+        step_bytes = step_bytes_of(nbytes)
 
         for _ in range(args.warmup):
             flush.fill_(1)
@@ -373,7 +391,7 @@ def run_ours(args, w):
 
         ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
         sampler = ClockSampler(local)
         with sampler:
             # keep the GPU busy for the sampler before and after the timed regions
@@ -404,7 +422,8 @@ def run_ours(args, w):
                 run_cached()
                 b.record(stream)
                 ev_cached.append((a, b))
-            # timed region 2: the same steps with an event between kernels (per-op times)
+            # timed region 2: per-op times, an event between calls; the separate
+            # layout and notify calls run first for comparison with the one call
             for i in range(args.steps):
                 flush.fill_(1)
                 e = ev[i]
@@ -413,10 +432,14 @@ def run_ours(args, w):
                 e[1].record(stream)
                 step.notify()
                 e[2].record(stream)
-                step.dispatch()
+                flush.fill_(1)
                 e[3].record(stream)
-                step.combine()
+                step.layout_notify()
                 e[4].record(stream)
+                step.dispatch()
+                e[5].record(stream)
+                step.combine()
+                e[6].record(stream)
             torch.cuda.synchronize(dev)
             t1 = time.time()
             pad_end = time.time() + 0.4
@@ -427,16 +450,16 @@ def run_ours(args, w):
         clocks = sampler.summary(t0 - 0.45, t1 + 0.45)
         assert ep.ep_sync_status(pipe.status, stream) == ep.EP_OK, "device status not OK after timing"
 
-    per = {k: [] for k in ("layout", "notify", "dispatch", "combine")}
+    per = {k: [] for k in ("layout", "notify", "layout_notify", "dispatch", "combine")}
     for e in ev:
-        for j, k in enumerate(per):
-            per[k].append(e[j].elapsed_time(e[j + 1]))
+        for k, (j0, j1) in zip(per, ((0, 1), (1, 2), (3, 4), (4, 5), (5, 6))):
+            per[k].append(e[j0].elapsed_time(e[j1]))
     steps_ms = [a.elapsed_time(b) for a, b in ev_step]
     ms_local = statistics.mean(steps_ms)
     ms = max_over_ranks(dist, ms_local)
     total_bytes = sum_over_ranks(dist, step_bytes)
     value = total_bytes / (ms * 1e-3) / 1e9
-    eager_ms = statistics.mean(e[0].elapsed_time(e[4]) for e in ev)
+    eager_ms = statistics.mean(e[3].elapsed_time(e[6]) for e in ev)
     cached_ms = max_over_ranks(dist, statistics.mean(a.elapsed_time(b) for a, b in ev_cached))
     tok = w.R * w.T
     cached_bytes = tok * 2 * w.H + P * 2 * w.H + P * (2 * w.H + 4) + tok * 2 * w.H
@@ -587,9 +610,11 @@ def run_ours(args, w):
                          "algorithmic_bytes_per_launch": nbytes[dom]},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4)},
-            "gpu_launches": 4 * args.steps,
-            "launch": ("CUDA graph replay of the four C-ABI calls" if graph is not None else
-                       "eager C-ABI calls") + "; kernels chained by programmatic dependent launch",
+            "gpu_launches": (3 if step.fused else 4) * args.steps,
+            "launch": ("CUDA graph replay of the three C-ABI calls" if graph is not None else
+                       "eager C-ABI calls") + " (ep_layout_notify " +
+                      ("as one kernel" if step.fused else "as two kernels") +
+                      ", ep_dispatch, ep_combine); kernels chained by programmatic dependent launch",
             "ms_per_step_eager_with_op_events": round(eager_ms, 5),
             "fp8_dispatch": fp8,
             "low_latency_layout": ll,

@@ -173,6 +173,68 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
                              ep::kDefaultWaitLimitNs, stream);
 }
 
+int32_t ep_layout_notify_fused(const ep_shape_t* shape) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return -1;
+    return ep::layout_notify_fused_ok(sh) ? 1 : 0;
+}
+
+ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
+                             int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank,
+                             int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                             int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+                             int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum,
+                             int32_t* recv_rdma_rank_prefix_sum, int32_t* recv_channel_offset,
+                             int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+                             int32_t* num_recv_tokens_per_expert, int64_t* recv_base,
+                             int32_t* send_pos, void* workspace, size_t workspace_bytes,
+                             int32_t* status, int32_t* host_num_recv_tokens, cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (!ep::array_ok(topk_idx, tokens * sh.K, 16) || !ep::aligned4(num_tokens_per_rank) ||
+        !ep::aligned4(num_tokens_per_rdma_rank) || !ep::aligned4(num_tokens_per_expert) ||
+        !ep::array_ok(is_token_in_rank, tokens * sh.R, 16) || !ep::array_ok(send_pos, tokens * sh.R, 16) ||
+        !ep::aligned4(status))
+        return EP_ERR_INVALID_ARG;
+    if (!ep::layout_notify_fused_ok(sh)) {
+        // two kernels: the layout step, then notify on its outputs
+        const ep_status_t st = ep_get_dispatch_layout(shape, topk_idx, num_tokens_per_rank,
+                                                      num_tokens_per_rdma_rank, num_tokens_per_expert,
+                                                      is_token_in_rank, status, stream);
+        if (st != EP_OK) return st;
+        return ep_notify_dispatch(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                  num_tokens_per_expert, rank_prefix_matrix, gbl_channel_prefix_matrix,
+                                  rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
+                                  recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
+                                  num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos,
+                                  workspace, workspace_bytes, status, host_num_recv_tokens, stream);
+    }
+    if (!ep::aligned4(rank_prefix_matrix) || !ep::aligned4(gbl_channel_prefix_matrix) ||
+        !ep::aligned4(rdma_channel_prefix_matrix) || !ep::aligned4(recv_gbl_rank_prefix_sum) ||
+        !ep::aligned4(recv_rdma_rank_prefix_sum) || !ep::aligned4(recv_channel_offset) ||
+        !ep::aligned4(num_recv_tokens) || !ep::aligned4(num_rdma_recv_tokens) ||
+        !ep::aligned4(num_recv_tokens_per_expert) || !ep::aligned8(recv_base))
+        return EP_ERR_INVALID_ARG;
+    if (host_num_recv_tokens != nullptr && !ep::aligned4(host_num_recv_tokens)) return EP_ERR_INVALID_ARG;
+    ep::NotifyArgs a = {};
+    a.rank_prefix_matrix = rank_prefix_matrix;
+    a.gbl_channel_prefix_matrix = gbl_channel_prefix_matrix;
+    a.rdma_channel_prefix_matrix = rdma_channel_prefix_matrix;
+    a.recv_gbl_rank_prefix_sum = recv_gbl_rank_prefix_sum;
+    a.recv_rdma_rank_prefix_sum = recv_rdma_rank_prefix_sum;
+    a.recv_channel_offset = recv_channel_offset;
+    a.num_recv_tokens = num_recv_tokens;
+    a.num_rdma_recv_tokens = num_rdma_recv_tokens;
+    a.num_recv_tokens_per_expert = num_recv_tokens_per_expert;
+    a.recv_base = recv_base;
+    a.send_pos = send_pos;
+    a.status = status;
+    a.host_num_recv_tokens = host_num_recv_tokens;
+    return ep::from_cuda(ep::launch_layout_notify(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                                  num_tokens_per_expert, is_token_in_rank, a, stream));
+}
+
 ep_status_t ep_notify_dispatch_noalloc(
     const ep_shape_t* shape, const uint8_t* is_token_in_rank, const int32_t* num_tokens_per_rank,
     const int32_t* num_tokens_per_rdma_rank, const int32_t* num_tokens_per_expert,

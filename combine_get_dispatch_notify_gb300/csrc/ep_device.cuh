@@ -155,6 +155,103 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---- cluster barrier split into its two halves ----
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// ---- per-token routing helpers (layout counting) ----
+
+__device__ __forceinline__ void count_expert(long long e, int E, int E_loc, int32_t* h_expert,
+                                             uint32_t& mask, bool& bad) {
+    if (e >= 0 && e < E) {
+        mask |= 1u << (static_cast<int>(e) / E_loc);
+        atomicAdd(&h_expert[e], 1);
+    } else if (e != -1) {
+        bad = true;
+    }
+}
+
+// Reads the K expert ids of one token, adds each valid id to the shared
+// expert histogram and returns the R-bit destination-rank mask (expert e lives
+// on rank e / E_loc).  An id outside [-1, E) sets `bad` and is ignored.  Up
+// to 16 ids are loaded before any is used, so their loads are in flight
+// together.  For even K the ids of a token start 16-byte aligned.
+__device__ __forceinline__ uint32_t token_rank_mask(const int64_t* ids, int K, int E, int E_loc,
+                                                    int32_t* h_expert, bool& bad) {
+    constexpr int kBatch = 16;
+    uint32_t mask = 0;
+    for (int k0 = 0; k0 < K; k0 += kBatch) {
+        const int n = min(K - k0, kBatch);
+        long long e[kBatch];
+        if ((K & 1) == 0) {
+#pragma unroll
+            for (int i = 0; i < kBatch / 2; ++i)
+                if (2 * i < n) {
+                    const longlong2 v = __ldg(reinterpret_cast<const longlong2*>(ids + k0) + i);
+                    e[2 * i] = v.x;
+                    e[2 * i + 1] = v.y;
+                }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if (i < n) e[i] = __ldg(ids + k0 + i);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            if (i < n) count_expert(e[i], E, E_loc, h_expert, mask, bad);
+    }
+    return mask;
+}
+
+// Hint: bring [p, p + bytes) into L2 with bulk prefetches issued by one
+// thread (the 16-byte-aligned interior; the ragged ends are left out).
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15u) & ~uintptr_t(15);
+    const uintptr_t b = (reinterpret_cast<uintptr_t>(p) + bytes) & ~uintptr_t(15);
+    constexpr uintptr_t kChunk = 1u << 16;
+    for (uintptr_t c = a; c < b; c += kChunk) {
+        const uint32_t n = static_cast<uint32_t>(b - c < kChunk ? b - c : kChunk);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c), "r"(n) : "memory");
+    }
+}
+
+// Rank mask -> node mask (node of rank r is r / 8).
+__device__ __forceinline__ uint32_t node_bits(uint32_t m, int R, int N) {
+    if (R <= kNodeSize) return m != 0u ? 1u : 0u;
+    uint32_t nm = 0;
+    for (int n = 0; n < N; ++n) nm |= ((m >> (kNodeSize * n)) & 0xffu) ? (1u << n) : 0u;
+    return nm;
+}
+
+// 4 mask bits -> 4 bytes holding 0 or 1 (bit i -> byte i, little-endian).
+__device__ __forceinline__ uint32_t bits4_to_bytes(uint32_t b) {
+    return (b & 1u) | ((b & 2u) << 7) | ((b & 4u) << 14) | ((b & 8u) << 21);
+}
+
+// Writes one is_token_in_rank row (R bytes of 0/1) from the rank mask.
+__device__ __forceinline__ void write_membership_row(uint8_t* row, uint32_t mask, int R) {
+    if ((R & 15) == 0) {
+        for (int w = 0; w < R / 16; ++w) {
+            const uint32_t m = mask >> (16 * w);
+            uint4 v;
+            v.x = bits4_to_bytes(m & 0xfu);
+            v.y = bits4_to_bytes((m >> 4) & 0xfu);
+            v.z = bits4_to_bytes((m >> 8) & 0xfu);
+            v.w = bits4_to_bytes((m >> 12) & 0xfu);
+            *reinterpret_cast<uint4*>(row + 16 * w) = v;
+        }
+    } else if ((R & 3) == 0) {
+        for (int w = 0; w < R / 4; ++w)
+            *reinterpret_cast<uint32_t*>(row + 4 * w) = bits4_to_bytes((mask >> (4 * w)) & 0xfu);
+    } else {
+        for (int r = 0; r < R; ++r) row[r] = static_cast<uint8_t>((mask >> r) & 1u);
+    }
+}
+
 }  // namespace ep
 
 namespace ep {
@@ -177,6 +274,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    if (cluster_x > 8) {  // above the portable cluster size
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};

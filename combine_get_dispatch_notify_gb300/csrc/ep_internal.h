@@ -59,6 +59,13 @@ cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace,
                           bool force_lookback, int stall_block, long long wait_limit_ns,
                           cudaStream_t stream);
 
+// Layout and notify in one launch (a cluster of R CTAs).  Usable when R <= 16,
+// T <= 8192 and such a cluster fits on the current device.
+bool layout_notify_fused_ok(const Shape& sh);
+cudaError_t launch_layout_notify(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+                                 int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                                 uint8_t* is_token_in_rank, const NotifyArgs& a, cudaStream_t stream);
+
 // x rows are H * x_elem_bytes bytes (2: bf16, 1: FP8); x_scales /
 // recv_x_scales ([tokens|rows][num_scales] fp32) may be NULL.
 cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, const float* x_scales,

@@ -22,30 +22,6 @@ constexpr int kLayoutThreads = 256;
 constexpr int kMaxClusterCtas = 8;       // portable cluster size
 constexpr int kTokensPerCtaTarget = 1024;
 
-// 4 mask bits -> 4 bytes holding 0 or 1 (bit i -> byte i, little-endian).
-__device__ __forceinline__ uint32_t bits4_to_bytes(uint32_t b) {
-    return (b & 1u) | ((b & 2u) << 7) | ((b & 4u) << 14) | ((b & 8u) << 21);
-}
-
-__device__ __forceinline__ void write_membership_row(uint8_t* row, uint32_t mask, int R) {
-    if ((R & 15) == 0) {
-        for (int w = 0; w < R / 16; ++w) {
-            const uint32_t m = mask >> (16 * w);
-            uint4 v;
-            v.x = bits4_to_bytes(m & 0xfu);
-            v.y = bits4_to_bytes((m >> 4) & 0xfu);
-            v.z = bits4_to_bytes((m >> 8) & 0xfu);
-            v.w = bits4_to_bytes((m >> 12) & 0xfu);
-            *reinterpret_cast<uint4*>(row + 16 * w) = v;
-        }
-    } else if ((R & 3) == 0) {
-        for (int w = 0; w < R / 4; ++w)
-            *reinterpret_cast<uint32_t*>(row + 4 * w) = bits4_to_bytes((mask >> (4 * w)) & 0xfu);
-    } else {
-        for (int r = 0; r < R; ++r) row[r] = static_cast<uint8_t>((mask >> r) & 1u);
-    }
-}
-
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, int N, int E_loc,
               int tokens_per_cta, int32_t* __restrict__ num_tokens_per_rank,
@@ -75,42 +51,10 @@ layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, 
         const int t = base + tid;
         uint32_t mask = 0;
         if (t < t_end) {
-            const int64_t* ids = topk_idx + (static_cast<int64_t>(s) * T + t) * K;
-            int k = 0;
-            if ((K & 1) == 0) {
-                for (; k < K; k += 2) {
-                    const longlong2 e2 = __ldg(reinterpret_cast<const longlong2*>(ids + k));
-                    const long long e[2] = {e2.x, e2.y};
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (e[h] >= 0 && e[h] < E) {
-                            mask |= 1u << static_cast<int>(e[h] / E_loc);
-                            atomicAdd(&h_expert[e[h]], 1);
-                        } else if (e[h] != -1) {
-                            bad = true;
-                        }
-                    }
-                }
-            } else {
-                for (; k < K; ++k) {
-                    const long long e = __ldg(ids + k);
-                    if (e >= 0 && e < E) {
-                        mask |= 1u << static_cast<int>(e / E_loc);
-                        atomicAdd(&h_expert[e], 1);
-                    } else if (e != -1) {
-                        bad = true;
-                    }
-                }
-            }
+            mask = token_rank_mask(topk_idx + (static_cast<int64_t>(s) * T + t) * K, K, E, E_loc, h_expert, bad);
             write_membership_row(is_token_in_rank + (static_cast<int64_t>(s) * T + t) * R, mask, R);
         }
-        uint32_t node_mask;
-        if (R <= kNodeSize) {
-            node_mask = mask != 0u ? 1u : 0u;
-        } else {
-            node_mask = 0;
-            for (int n = 0; n < N; ++n) node_mask |= ((mask >> (kNodeSize * n)) & 0xffu) ? (1u << n) : 0u;
-        }
+        const uint32_t node_mask = node_bits(mask, R, N);
         for (int r = 0; r < R; ++r) {
             const unsigned b = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
             if (lane == r) rank_acc += __popc(b);

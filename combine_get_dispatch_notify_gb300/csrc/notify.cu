@@ -100,13 +100,6 @@ __device__ __forceinline__ uint32_t load_mask(const uint8_t* row, int R) {
     return m;
 }
 
-__device__ __forceinline__ uint32_t node_bits(uint32_t m, int R, int N) {
-    if (R <= kNodeSize) return m != 0u ? 1u : 0u;
-    uint32_t nm = 0;
-    for (int n = 0; n < N; ++n) nm |= ((m >> (kNodeSize * n)) & 0xffu) ? (1u << n) : 0u;
-    return nm;
-}
-
 // Ticket 0: the per-rank results ([IN] sm0 stage 6), from the count inputs
 // only.  All inputs are loaded up front by many threads, then summed.
 __device__ void per_rank_results(const NotifyKernelArgs& p, int32_t* s_nrecv,

@@ -75,6 +75,8 @@ _SIGS = {
     "ep_dispatch_fp8": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i32] + [_vp] * 4 + [_i64] +
                         [_vp] * 6 + [_vp]),
     "ep_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i64] + [_vp] * 5 + [_vp]),
+    "ep_layout_notify": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_vp, _sz, _vp, _vp, _vp]),
+    "ep_layout_notify_fused": (_i32, [ctypes.POINTER(EpShape)]),
     "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 15 + [_vp, _vp, _vp]),
     "ep_ll_layout": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "ep_ll_dispatch": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
@@ -227,6 +229,41 @@ def ep_notify_dispatch(shape: EpShape, is_token_in_rank, num_tokens_per_rank,
                                   _sz(workspace.numel() * workspace.element_size()),
                                   _t(status, torch.int32, (1,), "status"), host, _stream(stream))
     _check("ep_notify_dispatch", rc)
+
+
+def ep_layout_notify_fused(shape: EpShape) -> int:
+    """1 when :func:`ep_layout_notify` runs as one kernel for ``shape`` on the
+    current device, 0 when it enqueues the two separate kernels."""
+    return int(lib().ep_layout_notify_fused(ctypes.byref(shape)))
+
+
+def ep_layout_notify(shape: EpShape, topk_idx, layout: dict, outs: dict, workspace, status,
+                     host_num_recv_tokens=None, stream=None) -> None:
+    """Layout and notify in one call.  ``layout`` holds the four layout outputs
+    (see :func:`alloc_layout`), ``outs`` the notify outputs (see
+    :func:`notify_shapes`); ``workspace`` as for :func:`ep_notify_dispatch`."""
+    R, T, K, E, N = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.num_experts, shape.N
+    shapes = notify_shapes(shape)
+    args = [_t(topk_idx, torch.int64, (R, T, K), "topk_idx"),
+            _t(layout["num_tokens_per_rank"], torch.int32, (R, R), "num_tokens_per_rank"),
+            _t(layout["num_tokens_per_rdma_rank"], torch.int32, (R, N), "num_tokens_per_rdma_rank"),
+            _t(layout["num_tokens_per_expert"], torch.int32, (R, E), "num_tokens_per_expert"),
+            _t(layout["is_token_in_rank"], torch.uint8, (R, T, R), "is_token_in_rank")]
+    for k in _NOTIFY_OUT:
+        shp, dt = shapes[k]
+        args.append(_t(outs[k], dt, shp, k))
+    need = ep_notify_workspace_bytes(shape)
+    if workspace is None or not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    host = _vp(None)
+    if host_num_recv_tokens is not None:
+        if host_num_recv_tokens.dtype != torch.int32 or host_num_recv_tokens.numel() < R + 1:
+            raise ValueError("host_num_recv_tokens must be int32 with R+1 elements")
+        host = _vp(host_num_recv_tokens.data_ptr())
+    rc = lib().ep_layout_notify(ctypes.byref(shape), *args, _vp(workspace.data_ptr()),
+                                _sz(workspace.numel() * workspace.element_size()),
+                                _t(status, torch.int32, (1,), "status"), host, _stream(stream))
+    _check("ep_layout_notify", rc)
 
 
 def ep_notify_dispatch_noalloc(shape: EpShape, is_token_in_rank, num_tokens_per_rank,
@@ -393,9 +430,10 @@ def alloc_combine(shape: EpShape, device="cuda") -> dict:
 
 @dataclass
 class Pipeline:
-    """Buffers for one shape plus the four calls in order (identity expert by
-    default).  Allocates once; :meth:`run` launches layout, notify, dispatch
-    and combine on the current stream without synchronising."""
+    """Buffers for one shape plus the four steps in order (identity expert by
+    default).  Allocates once; :meth:`run` launches layout + notify (one call,
+    :func:`ep_layout_notify`), dispatch and combine on the current stream
+    without synchronising."""
 
     shape: EpShape
     capacity_rows: int
@@ -410,11 +448,7 @@ class Pipeline:
 
     def run(self, x, topk_idx, topk_w, y=None, y_w=None, stream=None, host_num_recv_tokens=None):
         sh, L, Nt, D, C = self.shape, self.layout, self.notify, self.dispatch, self.combine
-        ep_get_dispatch_layout(sh, topk_idx, L["num_tokens_per_rank"], L["num_tokens_per_rdma_rank"],
-                               L["num_tokens_per_expert"], L["is_token_in_rank"], self.status, stream)
-        ep_notify_dispatch(sh, L["is_token_in_rank"], L["num_tokens_per_rank"],
-                           L["num_tokens_per_rdma_rank"], L["num_tokens_per_expert"], Nt,
-                           Nt["workspace"], self.status, host_num_recv_tokens, stream)
+        ep_layout_notify(sh, topk_idx, L, Nt, Nt["workspace"], self.status, host_num_recv_tokens, stream)
         ep_dispatch(sh, x, topk_idx, topk_w, Nt["send_pos"], Nt["recv_base"], D["recv_x"],
                     D["recv_topk_idx"], D["recv_topk_w"], D["recv_src_info"], self.status, stream)
         ep_combine(sh, D["recv_x"] if y is None else y, D["recv_topk_w"] if y_w is None else y_w,

@@ -202,6 +202,41 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
                                cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Steps 1 and 2 in one call: ep_get_dispatch_layout followed by
+ * ep_notify_dispatch on its outputs ([RT] getDispatchLayout then
+ * intranode/internodeNotifyDispatch; [IN] sm0 stages 3 and 6, sm1..x stages
+ * 1-3).  Every output of both calls is written, with the same values.
+ *
+ * When R <= 16, T <= 8192 and a thread-block cluster of R CTAs fits on the
+ * device, this is ONE kernel: CTA s counts source rank s's tokens and keeps
+ * one ballot word per 32 tokens and destination in shared memory; after a
+ * cluster barrier the cross-source sums are read from the other CTAs' shared
+ * memory, so there is no workspace traffic, no wait on another launch and no
+ * second pass over is_token_in_rank.  Otherwise it enqueues the two kernels
+ * of the separate calls.  ep_layout_notify_fused tells which.
+ *
+ * Arguments: topk_idx and the four layout outputs as for
+ * ep_get_dispatch_layout; the notify outputs, workspace (used only by the
+ * two-kernel form, but always required, zeroed once before first use) and
+ * host_num_recv_tokens as for ep_notify_dispatch.  send_pos must be 16-byte
+ * aligned.  An expert id outside [-1, E) sets EP_DEV_INPUT and is ignored.
+ */
+ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
+                             int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank,
+                             int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+                             int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+                             int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum,
+                             int32_t* recv_rdma_rank_prefix_sum, int32_t* recv_channel_offset,
+                             int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+                             int32_t* num_recv_tokens_per_expert, int64_t* recv_base,
+                             int32_t* send_pos, void* workspace, size_t workspace_bytes,
+                             int32_t* status, int32_t* host_num_recv_tokens, cudaStream_t stream);
+
+/* 1 when ep_layout_notify runs as one kernel for this shape on the current
+ * device, 0 when it enqueues two, -1 for an invalid shape. */
+int32_t ep_layout_notify_fused(const ep_shape_t* shape);
+
+/* ------------------------------------------------------------------------
  * ep_notify_dispatch without a caller-provided workspace.  The paper has no
  * counterpart; this exists for callers that cannot allocate device memory -
  * for example code running inside a host framework that owns every device

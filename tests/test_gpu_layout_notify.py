@@ -1,0 +1,130 @@
+"""ep_layout_notify (layout and notify in one call) vs the CPU oracle, element
+by element, through the C ABI: the one-kernel form on every shape it accepts
+(R <= 16, T <= 8192), the two-kernel form beyond, both bit-exact."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_get_dispatch_notify_gb300 import ep
+from combine_get_dispatch_notify_gb300.workloads import CONFIGS, Workload, gen_routing
+from gpu_util import check_layout_notify, shape_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ep.lib()
+
+
+def _fused_expected(w: Workload) -> int:
+    return 1 if (w.R <= 16 and w.T <= 8192) else 0
+
+
+def _run(w: Workload, idx: torch.Tensor, host=None):
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay = ep.alloc_layout(sh)
+    nt = ep.alloc_notify(sh)
+    # poison the outputs: every element must be written by the call
+    for d in (lay, nt):
+        for k, v in d.items():
+            if k != "workspace":
+                v.fill_(0x5A if v.dtype == torch.uint8 else -7)
+    ep.ep_layout_notify(sh, idx.cuda(), lay, nt, nt["workspace"], status, host)
+    return sh, lay, nt, status
+
+
+def _oracle(w: Workload, idx: torch.Tensor):
+    o = oracle.load()
+    lay = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+    nt = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay)
+    return lay, nt
+
+
+CASES = {
+    "tiny": CONFIGS["tiny"],
+    "low_latency": CONFIGS["low_latency"],
+    "prefill": CONFIGS["prefill"],
+    "skewed": CONFIGS["skewed"],  # R=16, T=8192: the largest one-kernel shape
+    "large": CONFIGS["large"],    # R=32: two kernels
+    "single_rank": Workload("e", R=1, T=37, H=64, E=6, K=3, C=4, routing="replace", mask=0.2),
+    "empty_tokens": Workload("e", R=4, T=0, H=64, E=8, K=2, C=3),
+    "channels_exceed_tokens": Workload("e", R=8, T=50, H=128, E=64, K=4, C=64, mask=0.1),
+    "odd_ranks_align": Workload("e", R=3, T=41, H=72, E=9, K=2, C=5, expert_alignment=4),
+    "ragged_tokens_r16": Workload("e", R=16, T=1001, H=64, E=256, K=7, C=13, routing="zipf", mask=0.05),
+    "max_experts": Workload("e", R=16, T=300, H=64, E=8192, K=9, C=4, routing="replace"),
+    "r5_odd_topk": Workload("e", R=5, T=257, H=64, E=40, K=5, C=9, mask=0.3),
+    "t8193_two_kernels": Workload("e", R=2, T=8193, H=64, E=16, K=2, C=3),
+    "r32_small": Workload("e", R=32, T=19, H=8, E=256, K=8, C=3, routing="replace", mask=0.3),
+    "all_masked": Workload("e", R=8, T=40, H=64, E=16, K=4, C=4, mask=1.0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_layout_notify_matches_oracle(name):
+    w = CASES[name]
+    idx, _ = gen_routing(w)
+    lay_ref, nt_ref = _oracle(w, idx)
+    sh, lay, nt, status = _run(w, idx)
+    assert ep.ep_layout_notify_fused(sh) == _fused_expected(w)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    check_layout_notify(lay, nt, lay_ref, nt_ref)
+    # a second call on the same buffers gives byte-identical results
+    snap = {k: v.clone() for k, v in {**lay, **nt}.items() if k != "workspace"}
+    ep.ep_layout_notify(sh, idx.cuda(), lay, nt, nt["workspace"], status)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    for k, v in snap.items():
+        assert torch.equal(v, {**lay, **nt}[k]), f"{k} differs between calls"
+
+
+def test_layout_notify_host_mapped_counts():
+    w = CONFIGS["low_latency"]
+    idx, _ = gen_routing(w)
+    _, nt_ref = _oracle(w, idx)
+    host = torch.zeros(w.R + 1, dtype=torch.int32).pin_memory()
+    sh, lay, nt, status = _run(w, idx, host)
+    torch.cuda.synchronize()
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    want = np.concatenate([nt_ref["num_recv_tokens"], [nt_ref["recv_base"][-1]]]).astype(np.int32)
+    assert np.array_equal(host.numpy(), want)
+
+
+def test_layout_notify_bad_expert_id_reports_status():
+    w = Workload("e", R=16, T=64, H=64, E=64, K=4, C=4)
+    idx, _ = gen_routing(w)
+    idx[3, 5, 1] = w.E + 7
+    idx[9, 0, 0] = -5
+    sh, lay, nt, status = _run(w, idx)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_INPUT
+    # the bad ids are ignored: the counts are those of the top-k without them
+    clean = idx.clone()
+    clean[3, 5, 1] = -1
+    clean[9, 0, 0] = -1
+    lay_ref, nt_ref = _oracle(w, clean)
+    check_layout_notify(lay, nt, lay_ref, nt_ref)
+
+
+def test_layout_notify_feeds_dispatch():
+    """The handle from the one-call form drives dispatch exactly like the
+    handle from the two separate calls."""
+    w = CONFIGS["low_latency"]
+    idx, wt = gen_routing(w)
+    o = oracle.load()
+    sh, lay, nt, status = _run(w, idx)
+    rows = int(nt["recv_base"][-1])
+    x = torch.randn(w.R, w.T, w.H, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    D = ep.alloc_dispatch(sh, rows)
+    ep.ep_dispatch(sh, x.cuda(), idx.cuda(), wt.cuda(), nt["send_pos"], nt["recv_base"], D["recv_x"],
+                   D["recv_topk_idx"], D["recv_topk_w"], D["recv_src_info"], status)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    lay_ref, nt_ref = _oracle(w, idx)
+    dp = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, x.view(torch.int16).numpy().view(np.uint16),
+                    idx.numpy(), wt.numpy(), nt_ref["send_pos"], nt_ref["recv_base"])
+    assert np.array_equal(D["recv_x"].view(torch.int16).cpu().numpy().view(np.uint16), dp["recv_x"])
+    assert np.array_equal(D["recv_src_info"].cpu().numpy(), dp["recv_src_info"])
