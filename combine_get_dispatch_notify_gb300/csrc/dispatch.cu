@@ -15,7 +15,9 @@
 //        armed, descriptor written) plus the copy's bytes;
 //   warp 1 (storer, one thread): waits "full", issues one bulk
 //        shared->global copy per destination, commits them as a bulk group,
-//        and frees the previous slot once its group has been read out;
+//        and frees the slot of the unit `lag` groups back once that group
+//        has been read out (up to 6 groups in flight, the rest of the ring
+//        is load-ahead);
 //   warps 2-3 (metadata): write recv_topk_idx / recv_topk_w / recv_src_info
 //        for the destination rows of each token with plain stores.
 // Each row is read from HBM once and written once per destination; no
@@ -33,6 +35,7 @@ constexpr int kMaxSlots = 16;
 constexpr int kCtasPerSm = 2;
 constexpr int kSmemBudget = 100 * 1024;   // per CTA: two CTAs per SM
 constexpr int kMaxPartBytes = 32 * 1024;
+constexpr int kStoreLag = 6;  // bulk store groups in flight per CTA
 
 struct SlotDesc {
     int n;               // destinations in rows[], -1 = end of stream
@@ -96,6 +99,18 @@ __device__ __forceinline__ long long lane_row(const DispatchArgs& p, const long 
         return -1;
     }
     return row;
+}
+
+// cp.async.bulk.wait_group.read takes an immediate: dispatch on the lag.
+__device__ __forceinline__ void bulk_wait_read_lag(int lag) {
+    switch (lag) {
+        case 1: bulk_wait_read<1>(); break;
+        case 2: bulk_wait_read<2>(); break;
+        case 3: bulk_wait_read<3>(); break;
+        case 4: bulk_wait_read<4>(); break;
+        case 5: bulk_wait_read<5>(); break;
+        default: bulk_wait_read<6>(); break;
+    }
 }
 
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs p) {
@@ -206,6 +221,10 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         }
     } else if (warp == 1) {
         // ---------------- storer ----------------
+        // Up to `lag` bulk groups stay in flight; the other slots are
+        // load-ahead for the producer, which waits for unit k - S's slot and
+        // so never for a unit it has not handed over (lag <= S - 1).
+        const int lag = S - 1 < kStoreLag ? S - 1 : kStoreLag;
         if (lane == 0) {
             for (int k = 0;; ++k) {
                 const int slot = k % S;
@@ -224,9 +243,9 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                     if (row >= 0) bulk_s2g(p.recv_x + row * p.row_bytes + off, src, bytes);
                 }
                 bulk_commit();
-                if (k >= 1) {
-                    bulk_wait_read<1>();
-                    mbar_arrive(&empty[(k - 1) % S]);
+                if (k >= lag) {  // unit k - lag's group has been read out: free its slot
+                    bulk_wait_read_lag(lag);
+                    mbar_arrive(&empty[(k - lag) % S]);
                 }
             }
             bulk_wait_all();
