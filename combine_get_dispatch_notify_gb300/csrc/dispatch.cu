@@ -32,8 +32,7 @@ namespace {
 
 constexpr int kDispatchThreads = 128;
 constexpr int kMaxSlots = 16;
-constexpr int kCtasPerSm = 2;
-constexpr int kSmemBudget = 100 * 1024;   // per CTA: two CTAs per SM
+constexpr int kSmemPerSm = 200 * 1024;    // ring bytes per SM, split over its CTAs
 constexpr int kMaxPartBytes = 32 * 1024;
 constexpr int kStoreLag = 6;  // bulk store groups in flight per CTA
 
@@ -316,15 +315,19 @@ namespace {
 cudaError_t launch_dispatch_args(DispatchArgs& p, long long tokens, cudaStream_t stream) {
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const long long grid_target = static_cast<long long>(sms) * kCtasPerSm;
     const long long row_bytes = p.row_bytes;
+    // Two CTAs (two storer threads) per SM for rows above 8 KB; three for
+    // smaller rows (FP8 at H = 7168), whose stores are too small for two
+    // threads to issue at full bandwidth.
+    const int ctas_per_sm = row_bytes <= 8192 ? 3 : 2;
+    const long long grid_target = static_cast<long long>(sms) * ctas_per_sm;
     // Row parts: at most 32 KB, and split further (down to 2 KB) while there
     // are fewer than 8 units per CTA.  Parts are multiples of 16 bytes.
     long long part = row_bytes < kMaxPartBytes ? row_bytes : kMaxPartBytes;
     auto units_for = [&](long long pb) { return tokens * ((row_bytes + pb - 1) / pb); };
     while (part > 2048 && units_for(part) < 8 * grid_target) part = ((part / 2) + 15) / 16 * 16;
     const int parts = static_cast<int>((row_bytes + part - 1) / part);
-    int slots = static_cast<int>(kSmemBudget / part);
+    int slots = static_cast<int>(kSmemPerSm / ctas_per_sm / part);
     slots = slots < 2 ? 2 : (slots > kMaxSlots ? kMaxSlots : slots);
     p.parts = parts;
     p.slots = slots;
