@@ -128,3 +128,77 @@ def test_layout_notify_feeds_dispatch():
                     idx.numpy(), wt.numpy(), nt_ref["send_pos"], nt_ref["recv_base"])
     assert np.array_equal(D["recv_x"].view(torch.int16).cpu().numpy().view(np.uint16), dp["recv_x"])
     assert np.array_equal(D["recv_src_info"].cpu().numpy(), dp["recv_src_info"])
+
+
+def test_layout_notify_first_call_inside_graph_capture():
+    """A shape never seen before is first called inside a CUDA-graph capture
+    (the one-kernel form's cluster-fit check runs then); replays match the oracle."""
+    w = Workload("e", R=6, T=77, H=64, E=48, K=3, C=5, mask=0.1)
+    idx, _ = gen_routing(w)
+    lay_ref, nt_ref = _oracle(w, idx)
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay, nt = ep.alloc_layout(sh), ep.alloc_notify(sh)
+    idx_d = idx.cuda()
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        ep.ep_layout_notify(sh, idx_d, lay, nt, nt["workspace"], status, stream=stream)
+    for _ in range(2):
+        for d in (lay, nt):
+            for k, v in d.items():
+                if k != "workspace":
+                    v.fill_(-3 if v.dtype != torch.uint8 else 7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert ep.ep_sync_status(status) == ep.EP_OK
+        check_layout_notify(lay, nt, lay_ref, nt_ref)
+    assert ep.ep_layout_notify_fused(sh) == 1
+
+
+@pytest.mark.parametrize("name", ["low_latency", "large_r32_small"])
+def test_pipeline_replayed_from_a_cuda_graph(name):
+    """The whole step captured once and replayed on new inputs copied into the
+    same buffers: every output matches the oracle for each replay."""
+    from combine_get_dispatch_notify_gb300.workloads import gen_x, worst_case_rows
+
+    w = CONFIGS["low_latency"] if name == "low_latency" else Workload(
+        "e", R=32, T=24, H=256, E=256, K=8, C=3, mask=0.1)  # two-kernel layout + notify
+    o = oracle.load()
+    sh = shape_of(w)
+    pipe = ep.Pipeline(sh, max(1, worst_case_rows(w)))
+    x_d = torch.empty(w.R, w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    idx_d = torch.empty(w.R, w.T, w.K, dtype=torch.int64, device="cuda")
+    wt_d = torch.empty(w.R, w.T, w.K, dtype=torch.float32, device="cuda")
+    idx0, wt0 = gen_routing(w)
+    idx_d.copy_(idx0)
+    wt_d.copy_(wt0)
+    x_d.copy_(gen_x(w))
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        pipe.run(x_d, idx_d, wt_d, stream=stream)  # eager call first, as a server would at start-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        cx, cw = pipe.run(x_d, idx_d, wt_d, stream=stream)
+    for seed in (11, 12):
+        ws = Workload(w.name, R=w.R, T=w.T, H=w.H, E=w.E, K=w.K, C=w.C, mask=w.mask, seed=seed)
+        idx, wt = gen_routing(ws)
+        x = gen_x(ws)
+        idx_d.copy_(idx)
+        wt_d.copy_(wt)
+        x_d.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        assert ep.ep_sync_status(pipe.status) == ep.EP_OK
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        lay, nt, dp, cb = oracle.run_all(w.R, w.T, w.K, w.E, w.H, w.C, w.expert_alignment, xb, idx.numpy(),
+                                         wt.numpy(), o)
+        check_layout_notify(pipe.layout, pipe.notify, lay, nt)
+        rows = int(nt["recv_base"][-1])
+        assert np.array_equal(pipe.dispatch["recv_x"][:rows].view(torch.int16).cpu().numpy().view(np.uint16),
+                              dp["recv_x"])
+        assert np.array_equal(pipe.dispatch["recv_src_info"][:rows].cpu().numpy(), dp["recv_src_info"])
+        assert np.array_equal(cx.view(torch.int16).cpu().numpy().view(np.uint16), cb["combined_x"])
+        assert np.array_equal(cw.cpu().numpy(), cb["combined_w"])
