@@ -201,8 +201,29 @@ def sum_over_ranks(dist, value: float) -> float:
 
 
 # ----------------------------------------------------------------------------- oracle arm
+def host_cpu() -> dict:
+    """Host cores and CPU model (the oracle runs single-threaded on one of them)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    import platform
+
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine()}
+
+
+LAST_ORACLE_OPS_MS: dict = {}
+
+
 def oracle_step_sample(w, budget_s: float, max_reps: int | None = None):
-    """Time the CPU oracle on the workload; returns (seconds per step, reps, P, note)."""
+    """Time the CPU oracle on the workload (each op timed on its own); returns
+    (seconds per step, reps, P).  Per-op means land in LAST_ORACLE_OPS_MS."""
     import oracle
 
     o = oracle.load()
@@ -210,16 +231,27 @@ def oracle_step_sample(w, budget_s: float, max_reps: int | None = None):
     x = gen_x(w).view(torch.int16).numpy().view(np.uint16)
     idx_np, wt_np = idx.numpy(), wt.numpy()
     times = []
+    ops = {k: [] for k in ("layout", "notify", "dispatch", "combine")}
     P = 0
     t_start = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        lay, nt, dp, cb = oracle.run_all(w.R, w.T, w.K, w.E, w.H, w.C, w.expert_alignment, x, idx_np,
-                                         wt_np, o)
-        times.append(time.perf_counter() - t0)
+        lay = o.layout(w.R, w.T, w.K, w.E, idx_np)
+        t1 = time.perf_counter()
+        nt = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay)
+        t2 = time.perf_counter()
+        dp = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, x, idx_np, wt_np, nt["send_pos"], nt["recv_base"])
+        t3 = time.perf_counter()
+        o.combine(w.R, w.T, w.K, w.H, dp["recv_x"], dp["recv_topk_w"], nt["send_pos"], nt["recv_base"])
+        t4 = time.perf_counter()
+        for k, a, b in (("layout", t0, t1), ("notify", t1, t2), ("dispatch", t2, t3), ("combine", t3, t4)):
+            ops[k].append(b - a)
+        times.append(t4 - t0)
         P = int(nt["recv_base"][-1])
         if time.perf_counter() - t_start >= budget_s or (max_reps and len(times) >= max_reps):
             break
+    LAST_ORACLE_OPS_MS.clear()
+    LAST_ORACLE_OPS_MS.update({k: round(statistics.mean(v) * 1e3, 3) for k, v in ops.items()})
     return statistics.mean(times), len(times), P
 
 
@@ -233,9 +265,11 @@ def run_reference(args, w):
     for _ in range(args.warmup):
         oracle_step_sample(w, 0.0, max_reps=1)
     t_all = time.perf_counter()
+    per_op = []
     for _ in range(args.steps):
         s, reps, P = oracle_step_sample(w, 0.0, max_reps=1)
         sec.append(s)
+        per_op.append(dict(LAST_ORACLE_OPS_MS))
         if time.perf_counter() - t_all > budget * 4:
             break
     step_s = statistics.mean(sec)
@@ -248,7 +282,9 @@ def run_reference(args, w):
         "data": "synthetic", "config": config_dict(w),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"whole {w.name} workload per step (all {w.R * w.T} tokens), "
-                                   f"single-threaded C oracle, {len(sec)} steps"},
+                                   f"single-threaded C oracle, {len(sec)} steps",
+                         "per_op_ms": {k: round(statistics.mean(d[k] for d in per_op), 3) for k in per_op[0]},
+                         "host": host_cpu()},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -591,7 +627,8 @@ def run_ours(args, w):
         cpu = {"value": round(step_bytes / sec / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"whole {w.name} workload ({tokens} tokens, all four steps) repeated "
                          f"{reps}x, single-threaded C oracle",
-               "ms_per_step": round(sec * 1e3, 2)}
+               "ms_per_step": round(sec * 1e3, 2), "per_op_ms": dict(LAST_ORACLE_OPS_MS),
+               "host": host_cpu()}
 
     if rank == 0:
         line = {
