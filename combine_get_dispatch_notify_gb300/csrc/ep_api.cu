@@ -1,6 +1,7 @@
 // C ABI of libep_gb300.so (declared in include/ep.h): argument checks on the
 // host, then one launch per step on the caller's stream.
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "ep.h"
@@ -14,6 +15,53 @@ int device_sm_count() {
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return sms;
+}
+
+namespace {
+struct FitKey {
+    const void* kernel;
+    int dev, cluster, threads;
+    size_t smem;
+    bool fits;
+};
+std::mutex g_fit_mu;
+FitKey g_fit_cache[128];
+int g_fit_count = 0;
+}  // namespace
+
+bool cluster_fits(const void* kernel, int cluster, int threads, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_fit_mu);
+    for (int i = 0; i < g_fit_count; ++i) {
+        const FitKey& k = g_fit_cache[i];
+        if (k.kernel == kernel && k.dev == dev && k.cluster == cluster && k.threads == threads && k.smem == smem)
+            return k.fits;
+    }
+    bool fits = true;
+    if (smem > 48 * 1024)
+        fits = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
+               cudaSuccess;
+    if (fits && cluster > 8)
+        fits = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    if (fits) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+        cfg.blockDim = dim3(static_cast<unsigned>(threads));
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        fits = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters > 0;
+        cudaGetLastError();  // a refused query leaves no sticky error behind
+    }
+    if (g_fit_count < 128) g_fit_cache[g_fit_count++] = FitKey{kernel, dev, cluster, threads, smem, fits};
+    return fits;
 }
 
 namespace {
@@ -365,10 +413,15 @@ ep_status_t ep_ll_layout(const ep_shape_t* shape, const int64_t* topk_idx,
     ep::Shape sh;
     if (!ep::make_shape(shape, &sh) || expert_capacity < 0) return EP_ERR_INVALID_ARG;
     const long long tokens = static_cast<long long>(sh.R) * sh.T;
-    if (!ep::array_ok(topk_idx, tokens * sh.K, 8) || !ep::aligned4(num_tokens_per_expert) ||
-        !ep::array_ok(slot_pos, tokens * sh.K, 4) || !ep::aligned4(layout_range) || !ep::aligned4(count) ||
-        !ep::aligned4(status))
+    if (!ep::array_ok(topk_idx, tokens * sh.K, 8) || !ep::array_ok(slot_pos, tokens * sh.K, 4) ||
+        !ep::aligned4(layout_range) || !ep::aligned4(count) || !ep::aligned4(status))
         return EP_ERR_INVALID_ARG;
+    if (num_tokens_per_expert == nullptr) {  // counting form: one cluster counts for itself
+        if (!ep::ll_layout_counting_ok(sh)) return EP_ERR_INVALID_ARG;
+        return ep::from_cuda(ep::launch_ll_layout_counting(sh, topk_idx, expert_capacity, slot_pos, layout_range,
+                                                           count, status, stream));
+    }
+    if (!ep::aligned4(num_tokens_per_expert)) return EP_ERR_INVALID_ARG;
     return ep::from_cuda(ep::launch_ll_layout(sh, topk_idx, num_tokens_per_expert, expert_capacity, slot_pos,
                                               layout_range, count, status, stream));
 }

@@ -17,6 +17,12 @@ struct Shape {
 // SM count of the current device (0 on error).
 int device_sm_count();
 
+// Whether one thread-block cluster of `cluster` CTAs of `kernel` (threads,
+// dynamic shared bytes) can be resident on the current device.  Asked once
+// per device and configuration, then cached; sets the kernel's attributes
+// (dynamic shared size above 48 KB, non-portable cluster size above 8).
+bool cluster_fits(const void* kernel, int cluster, int threads, size_t smem);
+
 cudaError_t launch_layout(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
                           int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
                           uint8_t* is_token_in_rank, int32_t* status, cudaStream_t stream);
@@ -85,6 +91,14 @@ cudaError_t launch_combine(const Shape& sh, const uint16_t* y, const float* y_w,
 cudaError_t launch_ll_layout(const Shape& sh, const int64_t* topk_idx, const int32_t* num_tokens_per_expert,
                              int cap, int32_t* slot_pos, int32_t* layout_range, int32_t* count,
                              int32_t* status, cudaStream_t stream);
+
+// The same without the per-expert count input: one cluster of R CTAs counts
+// and exchanges the per-source totals through distributed shared memory.
+// Usable when R <= 16, R * E <= 16384 and such a cluster fits.
+bool ll_layout_counting_ok(const Shape& sh);
+cudaError_t launch_ll_layout_counting(const Shape& sh, const int64_t* topk_idx, int cap, int32_t* slot_pos,
+                                      int32_t* layout_range, int32_t* count, int32_t* status,
+                                      cudaStream_t stream);
 
 // LL dispatch / combine share the dispatch and combine kernels; rows are
 // resolved from (topk_idx, slot_pos) as expert * cap + pos.

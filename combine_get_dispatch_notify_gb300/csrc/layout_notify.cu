@@ -34,8 +34,6 @@
 // same pass that builds is_token_in_rank, so they cannot disagree.
 #include <cooperative_groups.h>
 
-#include <mutex>
-
 #include "ep_device.cuh"
 #include "ep_internal.h"
 
@@ -298,58 +296,12 @@ int fused_threads(const Shape& sh) {
     return static_cast<int>(b < kMinThreads ? kMinThreads : (b > kMaxThreads ? kMaxThreads : b));
 }
 
-// Whether a cluster of R CTAs of this size can be resident on the current
-// device (asked once per device and configuration, then cached).
-struct FitKey {
-    int dev, R, threads;
-    size_t smem;
-    bool fits;
-};
-std::mutex g_fit_mu;
-FitKey g_fit_cache[64];
-int g_fit_count = 0;
-
-bool cluster_fits(int R, int threads, size_t smem) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    std::lock_guard<std::mutex> lock(g_fit_mu);
-    for (int i = 0; i < g_fit_count; ++i) {
-        const FitKey& k = g_fit_cache[i];
-        if (k.dev == dev && k.R == R && k.threads == threads && k.smem == smem) return k.fits;
-    }
-    bool fits = true;
-    if (smem > 48 * 1024)
-        fits = cudaFuncSetAttribute(layout_notify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem)) == cudaSuccess;
-    if (fits && R > 8)
-        fits = cudaFuncSetAttribute(layout_notify_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-               cudaSuccess;
-    if (fits) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(R));
-        cfg.blockDim = dim3(static_cast<unsigned>(threads));
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = static_cast<unsigned>(R);
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        fits = cudaOccupancyMaxActiveClusters(&clusters, layout_notify_kernel, &cfg) == cudaSuccess &&
-               clusters > 0;
-        cudaGetLastError();  // a refused query leaves no sticky error behind
-    }
-    if (g_fit_count < 64) g_fit_cache[g_fit_count++] = FitKey{dev, R, threads, smem, fits};
-    return fits;
-}
-
 }  // namespace
 
 bool layout_notify_fused_ok(const Shape& sh) {
     if (sh.R > kMaxRanks || sh.T > kMaxTokens) return false;
-    return cluster_fits(sh.R, fused_threads(sh), fused_smem_bytes(sh));
+    return cluster_fits(reinterpret_cast<const void*>(layout_notify_kernel), sh.R, fused_threads(sh),
+                        fused_smem_bytes(sh));
 }
 
 cudaError_t launch_layout_notify(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,

@@ -14,14 +14,26 @@
 // lowest lane advances the counter.  base(s,e) = slots that earlier source
 // ranks send to e, summed from num_tokens_per_expert.  Deterministic, no
 // global atomics, no waits.
+//
+// Counting form (no num_tokens_per_expert input): the R CTAs form one
+// thread-block cluster; after pass 1 each CTA stores its per-expert totals
+// into the shared memory of every later source's CTA (distributed shared
+// memory), and one cluster barrier later base(s,e) is summed from local
+// shared memory.
+#include <cooperative_groups.h>
+
 #include "ep_device.cuh"
 #include "ep_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace ep {
 namespace {
 
 constexpr int kLlThreads = 1024;
 constexpr int kCounterBudget = 48 * 1024;  // shared bytes for the per-warp counters
+constexpr int kMaxClusterRanks = 16;
+constexpr int kMaxExchangeInts = 16384;    // R * E totals exchanged in the counting form
 
 struct LlLayoutArgs {
     const int64_t* topk_idx;
@@ -33,8 +45,11 @@ struct LlLayoutArgs {
     int R, T, K, E, cap, warps;
 };
 
-__global__ void __launch_bounds__(kLlThreads) ll_layout_kernel(LlLayoutArgs p) {
-    extern __shared__ int32_t cnt[];  // [warps][E]
+// kCounting: base(s,e) from the cluster's exchanged totals instead of
+// num_tokens_per_expert (grid = one cluster of R CTAs).
+template <bool kCounting>
+__global__ void __launch_bounds__(kLlThreads, 1) ll_layout_kernel(LlLayoutArgs p) {
+    extern __shared__ int32_t cnt[];  // [warps][E], then (counting form) [R][E] totals
     const int s = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W = p.warps, E = p.E;
@@ -66,21 +81,43 @@ __global__ void __launch_bounds__(kLlThreads) ll_layout_kernel(LlLayoutArgs p) {
         }
     }
     __syncthreads();
-    // exclusive prefix over warps, per expert; ranges, totals, consistency
-    for (int e = tid; e < E; e += blockDim.x) {
-        int32_t run = 0;
-        for (int w = 0; w < W; ++w) {
-            const int32_t c = cnt[w * E + e];
-            cnt[w * E + e] = run;
-            run += c;
+    // exclusive prefix over warps, per expert; in the counting form this
+    // source's totals go to every later source's CTA, one cluster barrier
+    // later each CTA holds the totals of all earlier sources
+    int32_t* totals = cnt + W * E;  // counting form: [R][E], row s' = totals of source s'
+    if (kCounting) {
+        cg::cluster_group cluster = cg::this_cluster();
+        for (int e = tid; e < E; e += blockDim.x) {
+            int32_t run = 0;
+            for (int w = 0; w < W; ++w) {
+                const int32_t c = cnt[w * E + e];
+                cnt[w * E + e] = run;
+                run += c;
+            }
+            totals[s * E + e] = run;
+            for (int c = s + 1; c < p.R; ++c) cluster.map_shared_rank(totals, c)[s * E + e] = run;
         }
-        int32_t base = 0;
+        cluster.sync();
+    }
+    // ranges, totals, consistency
+    for (int e = tid; e < E; e += blockDim.x) {
+        int32_t run = 0, base = 0;
+        if (kCounting) {
+            run = totals[s * E + e];
+            for (int s2 = 0; s2 < s; ++s2) base += totals[s2 * E + e];
+        } else {
+            for (int w = 0; w < W; ++w) {
+                const int32_t c = cnt[w * E + e];
+                cnt[w * E + e] = run;
+                run += c;
+            }
 #pragma unroll 8
-        for (int s2 = 0; s2 < s; ++s2) base += __ldg(p.num_tokens_per_expert + static_cast<long long>(s2) * E + e);
+            for (int s2 = 0; s2 < s; ++s2) base += __ldg(p.num_tokens_per_expert + static_cast<long long>(s2) * E + e);
+            if (run != __ldg(p.num_tokens_per_expert + static_cast<long long>(s) * E + e))
+                flag_error(p.status, EP_DEV_INCONSISTENT);
+        }
         p.layout_range[(static_cast<long long>(e) * p.R + s) * 2 + 0] = base;
         p.layout_range[(static_cast<long long>(e) * p.R + s) * 2 + 1] = run;
-        if (run != __ldg(p.num_tokens_per_expert + static_cast<long long>(s) * E + e))
-            flag_error(p.status, EP_DEV_INCONSISTENT);
         if (s == p.R - 1) p.count[e] = base + run;
         // pass 2 starts every warp's counter at base + its prefix
         for (int w = 0; w < W; ++w) cnt[w * E + e] += base;
@@ -114,9 +151,15 @@ __global__ void __launch_bounds__(kLlThreads) ll_layout_kernel(LlLayoutArgs p) {
 
 }  // namespace
 
-cudaError_t launch_ll_layout(const Shape& sh, const int64_t* topk_idx, const int32_t* num_tokens_per_expert,
-                             int cap, int32_t* slot_pos, int32_t* layout_range, int32_t* count,
-                             int32_t* status, cudaStream_t stream) {
+namespace {
+
+int ll_warps(const Shape& sh) {
+    const int warps = kCounterBudget / static_cast<int>(sizeof(int32_t) * sh.E);
+    return warps < 1 ? 1 : (warps > kLlThreads / kWarp ? kLlThreads / kWarp : warps);
+}
+
+LlLayoutArgs ll_args(const Shape& sh, const int64_t* topk_idx, const int32_t* num_tokens_per_expert, int cap,
+                     int32_t* slot_pos, int32_t* layout_range, int32_t* count, int32_t* status) {
     LlLayoutArgs p;
     p.topk_idx = topk_idx;
     p.num_tokens_per_expert = num_tokens_per_expert;
@@ -129,11 +172,36 @@ cudaError_t launch_ll_layout(const Shape& sh, const int64_t* topk_idx, const int
     p.K = sh.K;
     p.E = sh.E;
     p.cap = cap;
-    int warps = kCounterBudget / static_cast<int>(sizeof(int32_t) * sh.E);
-    warps = warps < 1 ? 1 : (warps > kLlThreads / kWarp ? kLlThreads / kWarp : warps);
-    p.warps = warps;
-    const size_t smem = sizeof(int32_t) * static_cast<size_t>(warps) * sh.E;
-    return launch_pdl(ll_layout_kernel, dim3(sh.R), dim3(kLlThreads), smem, stream, 0, false, p);
+    p.warps = ll_warps(sh);
+    return p;
+}
+
+size_t ll_counting_smem(const Shape& sh) {
+    return sizeof(int32_t) * (static_cast<size_t>(ll_warps(sh)) + sh.R) * sh.E;
+}
+
+}  // namespace
+
+cudaError_t launch_ll_layout(const Shape& sh, const int64_t* topk_idx, const int32_t* num_tokens_per_expert,
+                             int cap, int32_t* slot_pos, int32_t* layout_range, int32_t* count,
+                             int32_t* status, cudaStream_t stream) {
+    const LlLayoutArgs p = ll_args(sh, topk_idx, num_tokens_per_expert, cap, slot_pos, layout_range, count, status);
+    const size_t smem = sizeof(int32_t) * static_cast<size_t>(p.warps) * sh.E;
+    return launch_pdl(ll_layout_kernel<false>, dim3(sh.R), dim3(kLlThreads), smem, stream, 0, false, p);
+}
+
+bool ll_layout_counting_ok(const Shape& sh) {
+    if (sh.R > kMaxClusterRanks || static_cast<long long>(sh.R) * sh.E > kMaxExchangeInts) return false;
+    return cluster_fits(reinterpret_cast<const void*>(ll_layout_kernel<true>), sh.R, kLlThreads,
+                        ll_counting_smem(sh));
+}
+
+cudaError_t launch_ll_layout_counting(const Shape& sh, const int64_t* topk_idx, int cap, int32_t* slot_pos,
+                                      int32_t* layout_range, int32_t* count, int32_t* status,
+                                      cudaStream_t stream) {
+    const LlLayoutArgs p = ll_args(sh, topk_idx, nullptr, cap, slot_pos, layout_range, count, status);
+    return launch_pdl(ll_layout_kernel<true>, dim3(sh.R), dim3(kLlThreads), ll_counting_smem(sh), stream,
+                      static_cast<unsigned>(sh.R), false, p);
 }
 
 }  // namespace ep

@@ -358,11 +358,13 @@ def ep_combine(shape: EpShape, y, y_w, send_pos, recv_base, combined_x, combined
 
 def ep_ll_layout(shape: EpShape, topk_idx, num_tokens_per_expert, expert_capacity: int, slot_pos,
                  layout_range, count, status, stream=None) -> None:
-    """Low-latency (per-expert packed) layout: row of each slot in its expert's buffer."""
+    """Low-latency (per-expert packed) layout: row of each slot in its expert's buffer.
+    ``num_tokens_per_expert`` may be None: the kernel then counts for itself (R <= 16)."""
     R, T, K, E = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.num_experts
     rc = lib().ep_ll_layout(
         ctypes.byref(shape), _t(topk_idx, torch.int64, (R, T, K), "topk_idx"),
-        _t(num_tokens_per_expert, torch.int32, (R, E), "num_tokens_per_expert"), _i32(expert_capacity),
+        _t(num_tokens_per_expert, torch.int32, (R, E), "num_tokens_per_expert", nullable=True),
+        _i32(expert_capacity),
         _t(slot_pos, torch.int32, (R, T, K), "slot_pos"), _t(layout_range, torch.int32, (E, R, 2), "layout_range"),
         _t(count, torch.int32, (E,), "count"), _t(status, torch.int32, (1,), "status"), _stream(stream))
     _check("ep_ll_layout", rc)

@@ -380,7 +380,14 @@ ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* 
  *
  * ep_ll_layout
  *   topk_idx               in  int64 [R][T][K]
- *   num_tokens_per_expert  in  int32 [R][E]  (from ep_get_dispatch_layout)
+ *   num_tokens_per_expert  in  int32 [R][E]  (from ep_get_dispatch_layout or
+ *                              ep_layout_notify), or NULL: then one
+ *                              thread-block cluster of R CTAs counts the
+ *                              slots itself and exchanges each source's
+ *                              per-expert totals through distributed shared
+ *                              memory.  NULL needs R <= 16, R*E <= 16384 and
+ *                              such a cluster to fit on the device, else
+ *                              EP_ERR_INVALID_ARG.
  *   expert_capacity        rows per expert buffer (>= 0)
  *   slot_pos               out int32 [R][T][K]  row in the slot's expert
  *                                                buffer, or -1
