@@ -9,9 +9,12 @@ the shape the dispatch/combine pages quote their latencies on.
 
 value   = algorithmic HBM bytes of the step / device time of the step (GB/s),
           inputs resident in HBM, L2 flushed (256 MB write) before every step;
-e2e     = the same bytes / time of the step done end to end from pinned host
+e2e     = the same bytes / time per step done end to end from pinned host
           buffers (H2D of x, top-k ids and weights; D2H of the combined rows
-          and weights) through the same C-ABI calls;
+          and weights every step) through the same C-ABI calls, pipelined as a
+          serving loop runs it (next step's inputs copied while this step
+          computes and returns); the one-step-at-a-time latency is reported
+          beside it;
 roofline: the dominant kernel (dispatch or combine) against the measured HBM
           copy bandwidth;
 cpu_baseline: the CPU oracle on the same workload (single thread).
@@ -302,7 +305,7 @@ class Step:
     pointers): ep_layout_notify, ep_dispatch, ep_combine; the separate layout and
     notify calls are kept for the per-op comparison."""
 
-    def __init__(self, ep, pipe, x, idx, wt, stream):
+    def __init__(self, ep, pipe, x, idx, wt, stream, combine=None):
         import ctypes
         self.ep = ep
         self.L = ep.lib()
@@ -310,7 +313,8 @@ class Step:
         self.sh = ctypes.byref(sh)
         v = ep._vp
         p = lambda t: v(t.data_ptr())  # noqa: E731
-        La, Nt, D, C = pipe.layout, pipe.notify, pipe.dispatch, pipe.combine
+        La, Nt, D = pipe.layout, pipe.notify, pipe.dispatch
+        C = pipe.combine if combine is None else combine
         s = v(stream.cuda_stream)
         st = p(pipe.status)
         self.layout_args = (self.sh, p(idx), p(La["num_tokens_per_rank"]), p(La["num_tokens_per_rdma_rank"]),
@@ -591,7 +595,14 @@ def run_ours(args, w):
                       ("ll_layout counting for itself" if counting else "layout + ll_layout") +
                       " + ll_dispatch + ll_combine (weighted), one CUDA graph"}
 
-    # end to end: pinned host inputs -> device -> the four calls -> host outputs
+    # End to end from pinned host buffers: every step copies its inputs (x, top-k
+    # ids and weights) host->device and its result (combined rows and weights)
+    # device->host, inside the timed region.  (1) synchronous: one step at a
+    # time, its latency; (2) pipelined, the way a serving loop runs: two sets
+    # of device inputs/outputs, later steps' inputs go up on one stream while
+    # step i computes (CUDA graph of the C-ABI calls, L2 flushed first) and its
+    # result comes down on a third stream; value = bytes / (wall time of K
+    # steps / K).
     x_h = x_d.cpu().pin_memory()
     idx_hp, wt_hp = idx_h.pin_memory(), wt_h.pin_memory()
     cx_h = torch.empty_like(pipe.combine["combined_x"], device="cpu").pin_memory()
@@ -614,8 +625,68 @@ def run_ours(args, w):
         b.synchronize()
         if i >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
-    e2e_ms_max = max_over_ranks(dist, statistics.mean(e2e_ms))
+    e2e_sync_ms = max_over_ranks(dist, statistics.mean(e2e_ms))
+
+    NB = 2  # device input/output sets in flight (a third gains nothing: the host link is the limit)
+    sets = []
+    for b in range(NB):
+        xb, ib, wb = torch.empty_like(x_d), torch.empty_like(idx_d), torch.empty_like(wt_d)
+        outb = ep.alloc_combine(sh, str(dev))
+        stb = Step(ep, pipe, xb, ib, wb, stream, combine=outb)
+        xb.copy_(x_d)
+        ib.copy_(idx_d)
+        wb.copy_(wt_d)
+        with torch.cuda.stream(stream):
+            stb.all()
+            gb = None
+            if graph is not None:
+                gb = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gb, stream=stream):
+                    stb.all()
+        sets.append((xb, ib, wb, outb, gb.replay if gb is not None else stb.all))
+    torch.cuda.synchronize(dev)
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(NB)]
+    ev_comp = [torch.cuda.Event() for _ in range(NB)]
+    ev_out = [torch.cuda.Event() for _ in range(NB)]
+
+    def issue(i):
+        b = i % NB
+        xb, ib, wb, outb, run_b = sets[b]
+        h2d_s.wait_event(ev_comp[b])  # step i-NB's compute has read this input set
+        with torch.cuda.stream(h2d_s):
+            xb.copy_(x_h, non_blocking=True)
+            ib.copy_(idx_hp, non_blocking=True)
+            wb.copy_(wt_hp, non_blocking=True)
+        ev_in[b].record(h2d_s)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # step i-NB's result has been read out of this output set
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            run_b()
+        ev_comp[b].record(stream)
+        d2h_s.wait_event(ev_comp[b])
+        with torch.cuda.stream(d2h_s):
+            cx_h.copy_(outb["combined_x"], non_blocking=True)
+            cw_h.copy_(outb["combined_w"], non_blocking=True)
+        ev_out[b].record(d2h_s)
+
+    for i in range(args.warmup):
+        issue(i)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_a.record(h2d_s)
+    for i in range(args.steps):
+        issue(i)
+    t_b.record(d2h_s)
+    torch.cuda.synchronize(dev)
+    e2e_ms_max = max_over_ranks(dist, t_a.elapsed_time(t_b) / args.steps)
     e2e_value = total_bytes / (e2e_ms_max * 1e-3) / 1e9
+    assert ep.ep_sync_status(pipe.status, stream) == ep.EP_OK, "device status not OK after the e2e legs"
+    e2e_ok = bool(torch.equal(sets[(args.steps - 1) % NB][3]["combined_x"].view(torch.int16),
+                              pipe.combine["combined_x"].view(torch.int16)))
+    torch.cuda.set_stream(torch.cuda.default_stream(dev))
 
     peak, peak_kind = measured_peak()
     dom = max(("dispatch", "combine"), key=lambda k: statistics.mean(per[k]))
@@ -656,7 +727,12 @@ def run_ours(args, w):
                          "traffic": recorded_traffic(dom, w.name),
                          "algorithmic_bytes_per_launch": nbytes[dom]},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4)},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4),
+                    "mode": "pipelined: two device input/output sets; each step's host->device copies, "
+                            "L2 flush + CUDA graph of the C-ABI calls, device->host copies on three streams",
+                    "sync_ms_per_step": round(e2e_sync_ms, 4),
+                    "sync_value": round(total_bytes / (e2e_sync_ms * 1e-3) / 1e9, 2),
+                    "result_matches_device_step": e2e_ok},
             "gpu_launches": (3 if step.fused else 4) * args.steps,
             "launch": ("CUDA graph replay of the three C-ABI calls" if graph is not None else
                        "eager C-ABI calls") + " (ep_layout_notify " +
