@@ -10,11 +10,66 @@
 
 namespace ep {
 
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_sm_mu;
+int g_sm_count[kMaxDevices] = {};
+
+struct KernelState {
+    const void* kernel;
+    int dev;
+    size_t smem_limit;  // dynamic shared bytes allowed so far
+    bool max_shared, nonportable;
+};
+std::mutex g_kernel_mu;
+KernelState g_kernels[256];
+int g_kernel_count = 0;
+}  // namespace
+
 int device_sm_count() {
-    int dev = 0, sms = 0;
+    int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_sm_mu);
+        if (g_sm_count[dev] > 0) return g_sm_count[dev];
+    }
+    int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_sm_mu);
+        g_sm_count[dev] = sms;
+    }
     return sms;
+}
+
+cudaError_t prepare_kernel(const void* kernel, size_t smem, bool max_shared, bool nonportable_cluster) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_kernel_mu);
+    KernelState* st = nullptr;
+    for (int i = 0; i < g_kernel_count; ++i)
+        if (g_kernels[i].kernel == kernel && g_kernels[i].dev == dev) st = &g_kernels[i];
+    KernelState fresh = {kernel, dev, 48 * 1024, false, false};
+    KernelState& k = st != nullptr ? *st : fresh;
+    if (max_shared && !k.max_shared) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        k.max_shared = true;
+    }
+    if (smem > k.smem_limit) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        k.smem_limit = smem;
+    }
+    if (nonportable_cluster && !k.nonportable) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        k.nonportable = true;
+    }
+    if (st == nullptr && g_kernel_count < 256) g_kernels[g_kernel_count++] = fresh;
+    return cudaSuccess;
 }
 
 namespace {
@@ -38,12 +93,8 @@ bool cluster_fits(const void* kernel, int cluster, int threads, size_t smem) {
         if (k.kernel == kernel && k.dev == dev && k.cluster == cluster && k.threads == threads && k.smem == smem)
             return k.fits;
     }
-    bool fits = true;
-    if (smem > 48 * 1024)
-        fits = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) ==
-               cudaSuccess;
-    if (fits && cluster > 8)
-        fits = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    // the same attribute cache as the launches, so the shared-memory limit only grows
+    bool fits = prepare_kernel(kernel, smem, false, cluster > 8) == cudaSuccess;
     if (fits) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(cluster));

@@ -256,6 +256,12 @@ __device__ __forceinline__ void write_membership_row(uint8_t* row, uint32_t mask
 
 namespace ep {
 
+// Host: sets what a launch of `kernel` with `smem` dynamic shared bytes needs
+// on the current device (the largest shared / smallest L1 split when
+// `max_shared`, the dynamic shared limit above 48 KB, non-portable cluster
+// sizes), once per kernel and device; later launches find it done.
+cudaError_t prepare_kernel(const void* kernel, size_t smem, bool max_shared, bool nonportable_cluster);
+
 // Host: launch `kernel` as a programmatic dependent of the previous work in
 // `stream` (its prologue may overlap the predecessor's tail).  `max_shared`
 // asks for the largest shared-memory / smallest L1 split (kernels that stage
@@ -265,21 +271,9 @@ template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, unsigned cluster_x, bool max_shared,
                               Args&&... args) {
-    cudaError_t e = cudaSuccess;
-    if (max_shared) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-    }
-    if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    if (cluster_x > 8) {  // above the portable cluster size
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
+    const cudaError_t e =
+        prepare_kernel(reinterpret_cast<const void*>(kernel), smem, max_shared, cluster_x > 8);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

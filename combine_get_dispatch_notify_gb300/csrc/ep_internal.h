@@ -20,7 +20,8 @@ int device_sm_count();
 // Whether one thread-block cluster of `cluster` CTAs of `kernel` (threads,
 // dynamic shared bytes) can be resident on the current device.  Asked once
 // per device and configuration, then cached; sets the kernel's attributes
-// (dynamic shared size above 48 KB, non-portable cluster size above 8).
+// through prepare_kernel (dynamic shared size above 48 KB, non-portable
+// cluster size above 8).
 bool cluster_fits(const void* kernel, int cluster, int threads, size_t smem);
 
 cudaError_t launch_layout(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
