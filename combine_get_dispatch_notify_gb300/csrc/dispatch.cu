@@ -322,10 +322,13 @@ cudaError_t launch_dispatch_args(DispatchArgs& p, long long tokens, cudaStream_t
     const int ctas_per_sm = row_bytes <= 8192 ? 3 : 2;
     const long long grid_target = static_cast<long long>(sms) * ctas_per_sm;
     // Row parts: at most 32 KB, and split further (down to 2 KB) while there
-    // are fewer than 8 units per CTA.  Parts are multiples of 16 bytes.
+    // are fewer than 8 units per CTA (4 for rows of 8 KB or less, whose
+    // halves are too small to pay for the extra units).  Parts are
+    // multiples of 16 bytes.
     long long part = row_bytes < kMaxPartBytes ? row_bytes : kMaxPartBytes;
     auto units_for = [&](long long pb) { return tokens * ((row_bytes + pb - 1) / pb); };
-    while (part > 2048 && units_for(part) < 8 * grid_target) part = ((part / 2) + 15) / 16 * 16;
+    const long long min_units = (row_bytes <= 8192 ? 4 : 8) * grid_target;
+    while (part > 2048 && units_for(part) < min_units) part = ((part / 2) + 15) / 16 * 16;
     const int parts = static_cast<int>((row_bytes + part - 1) / part);
     int slots = static_cast<int>(kSmemPerSm / ctas_per_sm / part);
     slots = slots < 2 ? 2 : (slots > kMaxSlots ? kMaxSlots : slots);
