@@ -66,6 +66,7 @@ struct DispatchArgs {
     long long row_bytes;
     long long num_units;
     long long wait_limit_ns;
+    int stall_release_cta;  // test hook: this CTA's storer never frees a slot (-1: none)
 };
 
 // Destination row this lane stands for, or -1: lane r = rank r through
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                 bulk_commit();
                 if (k >= lag) {  // unit k - lag's group has been read out: free its slot
                     bulk_wait_read_lag(lag);
-                    mbar_arrive(&empty[(k - lag) % S]);
+                    if (static_cast<int>(blockIdx.x) != p.stall_release_cta) mbar_arrive(&empty[(k - lag) % S]);
                 }
             }
             bulk_wait_all();
@@ -336,7 +337,6 @@ cudaError_t launch_dispatch_args(DispatchArgs& p, long long tokens, cudaStream_t
     p.slots = slots;
     p.part_bytes = static_cast<uint32_t>(part);
     p.num_units = tokens * parts;
-    p.wait_limit_ns = kDefaultWaitLimitNs;
     const size_t smem = static_cast<size_t>(slots) * part + 2 * slots * sizeof(uint64_t) +
                         slots * sizeof(SlotDesc) + 33 * sizeof(long long);
     const long long grid = p.num_units < grid_target ? p.num_units : grid_target;
@@ -347,6 +347,8 @@ cudaError_t launch_dispatch_args(DispatchArgs& p, long long tokens, cudaStream_t
 DispatchArgs base_args(const Shape& sh, int32_t* status) {
     DispatchArgs p = {};
     p.status = status;
+    p.wait_limit_ns = kDefaultWaitLimitNs;
+    p.stall_release_cta = -1;
     p.R = sh.R;
     p.T = sh.T;
     p.K = sh.K;
@@ -362,10 +364,12 @@ cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, co
                             const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
                             void* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, int stall_release_cta, long long wait_limit_ns) {
     const long long tokens = static_cast<long long>(sh.R) * sh.T;
     if (tokens == 0) return cudaSuccess;
     DispatchArgs p = base_args(sh, status);
+    p.stall_release_cta = stall_release_cta;
+    p.wait_limit_ns = wait_limit_ns;
     p.x = static_cast<const uint8_t*>(x);
     p.x_scales = x_scales;
     p.recv_x_scales = recv_x_scales;

@@ -203,6 +203,13 @@ ep_status_t notify_common(const ep_shape_t* shape, const uint8_t* is_token_in_ra
 }
 
 }  // namespace
+// Argument checks and launch shared by ep_dispatch and its stall test hook.
+ep_status_t dispatch_common(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
+                            const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
+                            int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                            float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                            cudaStream_t stream, int stall_cta, long long wait_limit_ns);
+
 }  // namespace ep
 
 extern "C" {
@@ -382,6 +389,31 @@ ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_
                         int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
                         float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
                         cudaStream_t stream) {
+    return ep::dispatch_common(shape, x, topk_idx, topk_w, send_pos, recv_base, capacity_rows, recv_x,
+                               recv_topk_idx, recv_topk_w, recv_src_info, status, stream, -1,
+                               ep::kDefaultWaitLimitNs);
+}
+
+ep_status_t ep_debug_dispatch_stall(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
+                                    const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
+                                    int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                                    float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                                    int32_t stall_cta, int32_t wait_limit_us, cudaStream_t stream) {
+    if (stall_cta < 0 || wait_limit_us < 1 || wait_limit_us > 2000000) return EP_ERR_INVALID_ARG;
+    return ep::dispatch_common(shape, x, topk_idx, topk_w, send_pos, recv_base, capacity_rows, recv_x,
+                               recv_topk_idx, recv_topk_w, recv_src_info, status, stream, stall_cta,
+                               static_cast<long long>(wait_limit_us) * 1000LL);
+}
+
+}  // extern "C"
+
+namespace ep {
+
+ep_status_t dispatch_common(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
+                            const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
+                            int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                            float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                            cudaStream_t stream, int stall_cta, long long wait_limit_ns) {
     ep::Shape sh;
     if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
     if (capacity_rows < 0) return EP_ERR_INVALID_ARG;
@@ -402,8 +434,12 @@ ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_
         return EP_ERR_INVALID_ARG;
     return ep::from_cuda(ep::launch_dispatch(sh, x, 2, nullptr, 0, topk_idx, topk_w, send_pos, recv_base,
                                              capacity_rows, recv_x, nullptr, recv_topk_idx, recv_topk_w,
-                                             recv_src_info, status, stream));
+                                             recv_src_info, status, stream, stall_cta, wait_limit_ns));
 }
+
+}  // namespace ep
+
+extern "C" {
 
 ep_status_t ep_dispatch_fp8(const ep_shape_t* shape, const uint8_t* x, const float* x_scales,
                             int32_t num_scales, const int64_t* topk_idx, const float* topk_w,

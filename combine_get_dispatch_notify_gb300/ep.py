@@ -84,6 +84,8 @@ _SIGS = {
     "ep_sync_status": (_i32, [_vp, _vp]),
     "ep_debug_notify_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 +
                                        [_sz, _vp, _i32, _i32, _vp]),
+    "ep_debug_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 5 +
+                                [_i32, _i32, _vp]),
 }
 
 _lib = None
@@ -316,6 +318,26 @@ def ep_dispatch(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x
         _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info", nullable=True),
         _t(status, torch.int32, (1,), "status"), _stream(stream))
     _check("ep_dispatch", rc)
+
+
+def ep_debug_dispatch_stall(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x, recv_topk_idx,
+                            recv_topk_w, recv_src_info, status, stall_cta: int, wait_limit_us: int,
+                            stream=None) -> None:
+    """Testing hook: ep_dispatch with CTA ``stall_cta`` never freeing a ring slot and
+    every device wait bounded by ``wait_limit_us``; the status word then reports a
+    timeout and the context stays usable."""
+    R, T, K, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.hidden
+    cap = _rows(recv_x, "recv_x")
+    rc = lib().ep_debug_dispatch_stall(
+        ctypes.byref(shape), _t(x, torch.bfloat16, (R, T, H), "x"),
+        _t(topk_idx, torch.int64, (R, T, K), "topk_idx"), _t(topk_w, torch.float32, (R, T, K), "topk_w"),
+        _t(send_pos, torch.int32, (R, T, R), "send_pos"), _t(recv_base, torch.int64, (R + 1,), "recv_base"),
+        _i64(cap), _t(recv_x, torch.bfloat16, (cap, H), "recv_x"),
+        _t(recv_topk_idx, torch.int64, (cap, K), "recv_topk_idx"),
+        _t(recv_topk_w, torch.float32, (cap, K), "recv_topk_w"),
+        _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info"), _t(status, torch.int32, (1,), "status"),
+        _i32(stall_cta), _i32(wait_limit_us), _stream(stream))
+    _check("ep_debug_dispatch_stall", rc)
 
 
 def ep_dispatch_fp8(shape: EpShape, x, x_scales, topk_idx, topk_w, send_pos, recv_base, recv_x,

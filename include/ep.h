@@ -442,6 +442,23 @@ ep_status_t ep_debug_notify_dispatch_stall(
     size_t workspace_bytes, int32_t* status, int32_t stall_block, int32_t wait_limit_us,
     cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Testing hook for failure detection in dispatch.  Runs ep_dispatch (same
+ * arguments) with CTA `stall_cta` withholding every ring-slot release and
+ * every device wait bounded by `wait_limit_us` microseconds (1 .. 2e6).  That
+ * CTA's producer gives up waiting for a free slot, its storer gives up
+ * waiting for the next unit, both set EP_DEV_TIMEOUT and the CTA exits after
+ * its in-flight bulk copies have completed, so the context stays usable.
+ * The other CTAs finish normally.  Output contents are undefined after such a
+ * run.  A shape whose CTAs all fit their units in the ring never waits for a
+ * slot, and then nothing times out.
+ */
+ep_status_t ep_debug_dispatch_stall(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
+                                    const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
+                                    int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                                    float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                                    int32_t stall_cta, int32_t wait_limit_us, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

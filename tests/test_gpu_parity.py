@@ -250,6 +250,36 @@ def test_stalled_lookback_times_out_and_context_survives():
     full_parity(CONFIGS["tiny"], random_expert=False)
 
 
+def test_stalled_dispatch_times_out_and_context_survives():
+    """A dispatch CTA whose storer never frees a ring slot: its producer's and
+    storer's bounded waits run out, the status word reports EP_ERR_TIMEOUT, the
+    other CTAs finish, and the next normal dispatch on the same buffers is
+    bit-exact."""
+    # 4 KB rows: 36 units for CTA 0 against a 16-slot ring, so its producer
+    # has to wait for a free slot
+    w = Workload("e", R=8, T=2048, H=2048, E=64, K=4, C=4)
+    idx, wt, x = make_inputs(w)
+    sh = shape_of(w)
+    o = oracle.load()
+    lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+    nt_ref = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref)
+    rows = int(nt_ref["recv_base"][-1])
+    sp, rb = torch.from_numpy(nt_ref["send_pos"]).cuda(), torch.from_numpy(nt_ref["recv_base"]).cuda()
+    D = ep.alloc_dispatch(sh, rows)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_debug_dispatch_stall(sh, x.cuda(), idx.cuda(), wt.cuda(), sp, rb, D["recv_x"], D["recv_topk_idx"],
+                               D["recv_topk_w"], D["recv_src_info"], status, stall_cta=0, wait_limit_us=2000)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_TIMEOUT
+    status.zero_()
+    ep.ep_dispatch(sh, x.cuda(), idx.cuda(), wt.cuda(), sp, rb, D["recv_x"], D["recv_topk_idx"], D["recv_topk_w"],
+                   D["recv_src_info"], status)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    dp = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, x.view(torch.int16).numpy().view(np.uint16), idx.numpy(),
+                    wt.numpy(), nt_ref["send_pos"], nt_ref["recv_base"])
+    assert_equal("recv_x after a stalled run", u16(D["recv_x"]), dp["recv_x"])
+    assert_equal("recv_src_info after a stalled run", D["recv_src_info"].cpu().numpy(), dp["recv_src_info"])
+
+
 def test_invalid_arguments_rejected_on_host():
     w = CONFIGS["tiny"]
     idx, wt, x = make_inputs(w)
