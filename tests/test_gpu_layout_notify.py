@@ -63,6 +63,11 @@ CASES = {
     "t8193_two_kernels": Workload("e", R=2, T=8193, H=64, E=16, K=2, C=3),
     "r32_small": Workload("e", R=32, T=19, H=8, E=256, K=8, C=3, routing="replace", mask=0.3),
     "all_masked": Workload("e", R=8, T=40, H=64, E=16, K=4, C=4, mask=1.0),
+    "k32_repeats": Workload("e", R=16, T=97, H=64, E=512, K=32, C=7, routing="replace", mask=0.1),
+    "c4096": Workload("e", R=4, T=300, H=64, E=16, K=2, C=4096, mask=0.2),
+    "one_token": Workload("e", R=16, T=1, H=64, E=16, K=3, C=1),
+    "one_expert_per_rank": Workload("e", R=16, T=200, H=64, E=16, K=5, C=3, routing="replace"),
+    "r8_t8192_e2048": Workload("e", R=8, T=8192, H=64, E=2048, K=8, C=24, routing="zipf"),
 }
 
 
