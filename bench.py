@@ -340,15 +340,16 @@ class Step:
                                    p(Nt["workspace"]), ep._sz(Nt["workspace"].numel()), st, v(None), s)
         self.fused = ep.ep_layout_notify_fused(sh) == 1
         cap = D["recv_x"].shape[0]
+        sc = p(pipe.sched)
         self.dispatch_args = (self.sh, p(x), p(idx), p(wt), p(Nt["send_pos"]), p(Nt["recv_base"]),
                               ep._i64(cap), p(D["recv_x"]), p(D["recv_topk_idx"]), p(D["recv_topk_w"]),
-                              p(D["recv_src_info"]), st, s)
+                              p(D["recv_src_info"]), st, sc, s)
         self.combine_args = (self.sh, p(D["recv_x"]), p(D["recv_topk_w"]), ep._i64(cap), p(Nt["send_pos"]),
                              p(Nt["recv_base"]), p(C["combined_x"]), p(C["combined_w"]), st, s)
         # cached mode: the handle (send_pos, recv_base) is reused, top-k not dispatched
         nul = v(None)
         self.dispatch_cached_args = (self.sh, p(x), nul, nul, p(Nt["send_pos"]), p(Nt["recv_base"]),
-                                     ep._i64(cap), p(D["recv_x"]), nul, nul, nul, st, s)
+                                     ep._i64(cap), p(D["recv_x"]), nul, nul, nul, st, sc, s)
         self.combine_cached_args = (self.sh, p(D["recv_x"]), nul, ep._i64(cap), p(Nt["send_pos"]),
                                     p(Nt["recv_base"]), p(C["combined_x"]), nul, st, s)
 
@@ -537,7 +538,8 @@ def run_ours(args, w):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 ep.ep_dispatch_fp8(sh, x8, xs8, idx_d, wt_d, Nt["send_pos"], Nt["recv_base"], rx8, rs8,
-                                   D["recv_topk_idx"], D["recv_topk_w"], D["recv_src_info"], pipe.status, stream)
+                                   D["recv_topk_idx"], D["recv_topk_w"], D["recv_src_info"], pipe.status, stream,
+                                   pipe.sched)
                 b.record(stream)
                 if i >= args.warmup:
                     f8_ms.append((a, b))
@@ -573,7 +575,7 @@ def run_ours(args, w):
                 ep.ep_get_dispatch_layout(sh, idx_d, La["num_tokens_per_rank"], La["num_tokens_per_rdma_rank"],
                                           La["num_tokens_per_expert"], La["is_token_in_rank"], pipe.status, stream)
                 ep.ep_ll_layout(sh, idx_d, La["num_tokens_per_expert"], cap, slot, rng_, cnt, pipe.status, stream)
-            ep.ep_ll_dispatch(sh, x_d, idx_d, slot, cap, rxl, srcl, pipe.status, stream)
+            ep.ep_ll_dispatch(sh, x_d, idx_d, slot, cap, rxl, srcl, pipe.status, stream, pipe.sched)
             ep.ep_ll_combine(sh, rxl, cap, idx_d, wt_d, slot, outl, pipe.status, stream)
 
         with torch.cuda.stream(stream):

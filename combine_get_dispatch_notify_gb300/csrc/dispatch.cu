@@ -67,6 +67,7 @@ struct DispatchArgs {
     long long num_units;
     long long wait_limit_ns;
     int stall_release_cta;  // test hook: this CTA's storer never frees a slot (-1: none)
+    unsigned long long* sched;  // unit counter (dynamic assignment), or NULL (static)
 };
 
 // Destination row this lane stands for, or -1: lane r = rank r through
@@ -134,9 +135,25 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     __syncthreads();
     // x is an input of the step, not written by layout or notify, so the
     // first ring-full of row parts is loaded while notify is still running.
+    // Unit assignment.  Static: CTA b takes units b, b + grid, ...
+    // Dynamic (counter): CTA b takes its first P0 units that way (they are the
+    // ones loaded before the dependency wait), and every later unit from the
+    // counter, so CTAs on faster SMs take more of them.  Each CTA's producer
+    // keeps one counter grab in flight and ends on exactly one grab past the
+    // end; the grab that sees the last value of the call resets the counter,
+    // so every call leaves it zero for the next.
+    // With fewer units per CTA than ring slots there is (almost) nothing left
+    // to balance after the first ring-full, and the counter's grabs would only
+    // add their latency: such calls keep the static split.
+    const long long per_cta = p.num_units / gridDim.x;
+    const bool dynamic = p.sched != nullptr && per_cta > S;
     const long long units_here =
         blockIdx.x < p.num_units ? (p.num_units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    const int pre = units_here < S ? static_cast<int>(units_here) : S;
+    const long long P0 = dynamic ? (per_cta < S ? per_cta : S) : units_here;
+    const int pre = static_cast<int>(P0 < S ? P0 : S);
+    const unsigned long long dyn_units =
+        dynamic ? static_cast<unsigned long long>(p.num_units - P0 * gridDim.x) : 0ull;
+    const unsigned long long last_grab = dyn_units + gridDim.x - 1;  // value of the call's final grab
     if (warp == 0 && lane == 0) {
         long long u = blockIdx.x;
         for (int i = 0; i < pre; ++i, u += gridDim.x) {
@@ -157,7 +174,33 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         // ---------------- producer ----------------
         int k = 0;  // units (then the end marker) handed to the storer
         bool ok = true;
-        for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        unsigned long long grab = 0;  // lane 0: value of the counter grab in flight
+        bool grab_pending = false;
+        if (dynamic && lane == 0) {
+            grab = atomicAdd(p.sched, 1ull);  // in flight while the static units are handed over
+            grab_pending = true;
+        }
+        for (;;) {
+            long long u;
+            if (k < P0) {
+                u = blockIdx.x + static_cast<long long>(k) * gridDim.x;
+            } else if (!dynamic) {
+                break;
+            } else {
+                unsigned long long got = grab;
+                if (lane == 0) {
+                    grab_pending = false;
+                    if (got == last_grab) {
+                        atomicExch(p.sched, 0ull);
+                    } else if (got < dyn_units) {
+                        grab = atomicAdd(p.sched, 1ull);  // the next one, in flight during this unit
+                        grab_pending = true;
+                    }
+                }
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (got >= dyn_units) break;
+                u = P0 * gridDim.x + static_cast<long long>(got);
+            }
             const long long g = u / p.parts;
             const int part = static_cast<int>(u - g * p.parts);
             const long long row = lane_row(p, base, g, lane);
@@ -208,6 +251,19 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         }
         if (lane == 0) {
             if (!ok) flag_error(p.status, EP_DEV_TIMEOUT);
+            // A wait that ran out left this CTA's grabs unfinished: keep grabbing
+            // (the units are left undone) until one lands past the end, so the
+            // call's grab count, and with it the counter reset, stay exact.
+            while (grab_pending) {
+                if (grab == last_grab) {
+                    atomicExch(p.sched, 0ull);
+                    grab_pending = false;
+                } else if (grab >= dyn_units) {
+                    grab_pending = false;
+                } else {
+                    grab = atomicAdd(p.sched, 1ull);
+                }
+            }
             // Drain: the newest phase armed on each slot has completed, so no
             // bulk copy into shared memory outlives the CTA.  (A wait can only
             // run out after every prefetched unit was handed over, so no phase
@@ -349,6 +405,7 @@ DispatchArgs base_args(const Shape& sh, int32_t* status) {
     p.status = status;
     p.wait_limit_ns = kDefaultWaitLimitNs;
     p.stall_release_cta = -1;
+    p.sched = nullptr;
     p.R = sh.R;
     p.T = sh.T;
     p.K = sh.K;
@@ -364,10 +421,12 @@ cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, co
                             const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
                             void* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                            cudaStream_t stream, int stall_release_cta, long long wait_limit_ns) {
+                            unsigned long long* sched, cudaStream_t stream, int stall_release_cta,
+                            long long wait_limit_ns) {
     const long long tokens = static_cast<long long>(sh.R) * sh.T;
     if (tokens == 0) return cudaSuccess;
     DispatchArgs p = base_args(sh, status);
+    p.sched = sched;
     p.stall_release_cta = stall_release_cta;
     p.wait_limit_ns = wait_limit_ns;
     p.x = static_cast<const uint8_t*>(x);
@@ -389,10 +448,12 @@ cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, co
 
 cudaError_t launch_ll_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
                                const int32_t* slot_pos, int cap, uint16_t* recv_x,
-                               int32_t* recv_src_info, int32_t* status, cudaStream_t stream) {
+                               int32_t* recv_src_info, int32_t* status, unsigned long long* sched,
+                               cudaStream_t stream) {
     const long long tokens = static_cast<long long>(sh.R) * sh.T;
     if (tokens == 0) return cudaSuccess;
     DispatchArgs p = base_args(sh, status);
+    p.sched = sched;
     p.x = reinterpret_cast<const uint8_t*>(x);
     p.topk_idx = topk_idx;
     p.ll_slot_pos = slot_pos;

@@ -208,7 +208,7 @@ ep_status_t dispatch_common(const ep_shape_t* shape, const uint16_t* x, const in
                             const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
                             int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                            cudaStream_t stream, int stall_cta, long long wait_limit_ns);
+                            uint64_t* sched, cudaStream_t stream, int stall_cta, long long wait_limit_ns);
 
 }  // namespace ep
 
@@ -387,10 +387,10 @@ ep_status_t ep_debug_notify_dispatch_stall(
 ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
                         const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
                         int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
-                        float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                        float* recv_topk_w, int32_t* recv_src_info, int32_t* status, uint64_t* sched,
                         cudaStream_t stream) {
     return ep::dispatch_common(shape, x, topk_idx, topk_w, send_pos, recv_base, capacity_rows, recv_x,
-                               recv_topk_idx, recv_topk_w, recv_src_info, status, stream, -1,
+                               recv_topk_idx, recv_topk_w, recv_src_info, status, sched, stream, -1,
                                ep::kDefaultWaitLimitNs);
 }
 
@@ -398,10 +398,11 @@ ep_status_t ep_debug_dispatch_stall(const ep_shape_t* shape, const uint16_t* x, 
                                     const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
                                     int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
                                     float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                                    int32_t stall_cta, int32_t wait_limit_us, cudaStream_t stream) {
+                                    uint64_t* sched, int32_t stall_cta, int32_t wait_limit_us,
+                                    cudaStream_t stream) {
     if (stall_cta < 0 || wait_limit_us < 1 || wait_limit_us > 2000000) return EP_ERR_INVALID_ARG;
     return ep::dispatch_common(shape, x, topk_idx, topk_w, send_pos, recv_base, capacity_rows, recv_x,
-                               recv_topk_idx, recv_topk_w, recv_src_info, status, stream, stall_cta,
+                               recv_topk_idx, recv_topk_w, recv_src_info, status, sched, stream, stall_cta,
                                static_cast<long long>(wait_limit_us) * 1000LL);
 }
 
@@ -413,7 +414,7 @@ ep_status_t dispatch_common(const ep_shape_t* shape, const uint16_t* x, const in
                             const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
                             int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                            cudaStream_t stream, int stall_cta, long long wait_limit_ns) {
+                            uint64_t* sched, cudaStream_t stream, int stall_cta, long long wait_limit_ns) {
     ep::Shape sh;
     if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
     if (capacity_rows < 0) return EP_ERR_INVALID_ARG;
@@ -430,11 +431,14 @@ ep_status_t dispatch_common(const ep_shape_t* shape, const uint16_t* x, const in
         return EP_ERR_INVALID_ARG;
     if (!ep::array_ok(x, tokens * sh.H, 16) || !ep::array_ok(send_pos, tokens * sh.R, 4) ||
         !ep::aligned8(recv_base) || !ep::array_ok(recv_x, cap * sh.H, 16) ||
-        (recv_src_info != nullptr && !ep::aligned8(recv_src_info)) || !ep::aligned4(status))
+        (recv_src_info != nullptr && !ep::aligned8(recv_src_info)) || !ep::aligned4(status) ||
+        (sched != nullptr && !ep::aligned8(sched)))
         return EP_ERR_INVALID_ARG;
     return ep::from_cuda(ep::launch_dispatch(sh, x, 2, nullptr, 0, topk_idx, topk_w, send_pos, recv_base,
                                              capacity_rows, recv_x, nullptr, recv_topk_idx, recv_topk_w,
-                                             recv_src_info, status, stream, stall_cta, wait_limit_ns));
+                                             recv_src_info, status,
+                                             reinterpret_cast<unsigned long long*>(sched), stream, stall_cta,
+                                             wait_limit_ns));
 }
 
 }  // namespace ep
@@ -446,9 +450,10 @@ ep_status_t ep_dispatch_fp8(const ep_shape_t* shape, const uint8_t* x, const flo
                             const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
                             uint8_t* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                            cudaStream_t stream) {
+                            uint64_t* sched, cudaStream_t stream) {
     ep::Shape sh;
     if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    if (sched != nullptr && !ep::aligned8(sched)) return EP_ERR_INVALID_ARG;
     if (capacity_rows < 0 || sh.H % 16 != 0 || num_scales < 0 || num_scales > 4096) return EP_ERR_INVALID_ARG;
     const long long tokens = static_cast<long long>(sh.R) * sh.T;
     const long long cap = capacity_rows;
@@ -470,7 +475,8 @@ ep_status_t ep_dispatch_fp8(const ep_shape_t* shape, const uint8_t* x, const flo
     return ep::from_cuda(ep::launch_dispatch(sh, x, 1, num_scales > 0 ? x_scales : nullptr, num_scales,
                                              topk_idx, topk_w, send_pos, recv_base, capacity_rows, recv_x,
                                              num_scales > 0 ? recv_x_scales : nullptr, recv_topk_idx,
-                                             recv_topk_w, recv_src_info, status, stream));
+                                             recv_topk_w, recv_src_info, status,
+                                             reinterpret_cast<unsigned long long*>(sched), stream));
 }
 
 ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* y_w,
@@ -515,9 +521,10 @@ ep_status_t ep_ll_layout(const ep_shape_t* shape, const int64_t* topk_idx,
 
 ep_status_t ep_ll_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
                            const int32_t* slot_pos, int32_t expert_capacity, uint16_t* recv_x,
-                           int32_t* recv_src_info, int32_t* status, cudaStream_t stream) {
+                           int32_t* recv_src_info, int32_t* status, uint64_t* sched, cudaStream_t stream) {
     ep::Shape sh;
     if (!ep::make_shape(shape, &sh) || expert_capacity < 0) return EP_ERR_INVALID_ARG;
+    if (sched != nullptr && !ep::aligned8(sched)) return EP_ERR_INVALID_ARG;
     const long long tokens = static_cast<long long>(sh.R) * sh.T;
     const long long rows = static_cast<long long>(sh.E) * expert_capacity;
     if (!ep::array_ok(x, tokens * sh.H, 16) || !ep::array_ok(topk_idx, tokens * sh.K, 8) ||
@@ -525,7 +532,8 @@ ep_status_t ep_ll_dispatch(const ep_shape_t* shape, const uint16_t* x, const int
         (recv_src_info != nullptr && !ep::aligned8(recv_src_info)) || !ep::aligned4(status))
         return EP_ERR_INVALID_ARG;
     return ep::from_cuda(ep::launch_ll_dispatch(sh, x, topk_idx, slot_pos, expert_capacity, recv_x,
-                                                recv_src_info, status, stream));
+                                                recv_src_info, status,
+                                                reinterpret_cast<unsigned long long*>(sched), stream));
 }
 
 ep_status_t ep_ll_combine(const ep_shape_t* shape, const uint16_t* y, int32_t expert_capacity,

@@ -77,12 +77,14 @@ cudaError_t launch_layout_notify(const Shape& sh, const int64_t* topk_idx, int32
 // recv_x_scales ([tokens|rows][num_scales] fp32) may be NULL.
 // stall_release_cta >= 0 (test hook): that CTA's storer never frees a ring
 // slot, so its producer's bounded wait runs out (EP_DEV_TIMEOUT).
+// sched: 8-byte unit counter for dynamic assignment (zero before the call,
+// zero after it), or NULL for the static split.
 cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, const float* x_scales,
                             int num_scales, const int64_t* topk_idx, const float* topk_w,
                             const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
                             void* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                            cudaStream_t stream, int stall_release_cta = -1,
+                            unsigned long long* sched, cudaStream_t stream, int stall_release_cta = -1,
                             long long wait_limit_ns = 1000000000LL);
 
 cudaError_t launch_combine(const Shape& sh, const uint16_t* y, const float* y_w, int64_t y_rows,
@@ -108,7 +110,8 @@ cudaError_t launch_ll_layout_counting(const Shape& sh, const int64_t* topk_idx, 
 // resolved from (topk_idx, slot_pos) as expert * cap + pos.
 cudaError_t launch_ll_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,
                                const int32_t* slot_pos, int cap, uint16_t* recv_x,
-                               int32_t* recv_src_info, int32_t* status, cudaStream_t stream);
+                               int32_t* recv_src_info, int32_t* status, unsigned long long* sched,
+                               cudaStream_t stream);
 cudaError_t launch_ll_combine(const Shape& sh, const uint16_t* y, int cap, const int64_t* topk_idx,
                               const float* topk_w, const int32_t* slot_pos, uint16_t* combined_x,
                               int32_t* status, cudaStream_t stream);

@@ -71,20 +71,20 @@ _SIGS = {
     "ep_notify_workspace_bytes": (_sz, [ctypes.POINTER(EpShape)]),
     "ep_get_dispatch_layout": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 6 + [_vp]),
     "ep_notify_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_sz, _vp, _vp, _vp]),
-    "ep_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 5 + [_vp]),
+    "ep_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 6 + [_vp]),
     "ep_dispatch_fp8": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i32] + [_vp] * 4 + [_i64] +
-                        [_vp] * 6 + [_vp]),
+                        [_vp] * 7 + [_vp]),
     "ep_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i64] + [_vp] * 5 + [_vp]),
     "ep_layout_notify": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_vp, _sz, _vp, _vp, _vp]),
     "ep_layout_notify_fused": (_i32, [ctypes.POINTER(EpShape)]),
     "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 15 + [_vp, _vp, _vp]),
     "ep_ll_layout": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
-    "ep_ll_dispatch": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "ep_ll_dispatch": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "ep_ll_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ep_sync_status": (_i32, [_vp, _vp]),
     "ep_debug_notify_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 +
                                        [_sz, _vp, _i32, _i32, _vp]),
-    "ep_debug_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 5 +
+    "ep_debug_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 5 + [_i64] + [_vp] * 6 +
                                 [_i32, _i32, _vp]),
 }
 
@@ -300,10 +300,16 @@ def ep_debug_notify_dispatch_stall(shape: EpShape, is_token_in_rank, num_tokens_
     _check("ep_debug_notify_dispatch_stall", rc)
 
 
+def _sched(sched):
+    return _t(sched, torch.int64, (1,), "sched", nullable=True)
+
+
 def ep_dispatch(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x, recv_topk_idx,
-                recv_topk_w, recv_src_info, status, stream=None) -> None:
+                recv_topk_w, recv_src_info, status, stream=None, sched=None) -> None:
     """Cached mode: pass topk_idx, topk_w, recv_topk_idx and recv_topk_w as None
-    (and recv_src_info optionally) to reuse an earlier notify handle."""
+    (and recv_src_info optionally) to reuse an earlier notify handle.  ``sched``: an
+    int64 CUDA tensor of one element, zero before the first call (the calls keep it
+    zero), for dynamic assignment of row parts to CTAs; None keeps the static split."""
     R, T, K, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.hidden
     cap = _rows(recv_x, "recv_x")
     rc = lib().ep_dispatch(
@@ -316,13 +322,13 @@ def ep_dispatch(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x
         _t(recv_topk_idx, torch.int64, (cap, K), "recv_topk_idx", nullable=True),
         _t(recv_topk_w, torch.float32, (cap, K), "recv_topk_w", nullable=True),
         _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info", nullable=True),
-        _t(status, torch.int32, (1,), "status"), _stream(stream))
+        _t(status, torch.int32, (1,), "status"), _sched(sched), _stream(stream))
     _check("ep_dispatch", rc)
 
 
 def ep_debug_dispatch_stall(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x, recv_topk_idx,
                             recv_topk_w, recv_src_info, status, stall_cta: int, wait_limit_us: int,
-                            stream=None) -> None:
+                            stream=None, sched=None) -> None:
     """Testing hook: ep_dispatch with CTA ``stall_cta`` never freeing a ring slot and
     every device wait bounded by ``wait_limit_us``; the status word then reports a
     timeout and the context stays usable."""
@@ -336,14 +342,16 @@ def ep_debug_dispatch_stall(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_
         _t(recv_topk_idx, torch.int64, (cap, K), "recv_topk_idx"),
         _t(recv_topk_w, torch.float32, (cap, K), "recv_topk_w"),
         _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info"), _t(status, torch.int32, (1,), "status"),
-        _i32(stall_cta), _i32(wait_limit_us), _stream(stream))
+        _sched(sched), _i32(stall_cta), _i32(wait_limit_us), _stream(stream))
     _check("ep_debug_dispatch_stall", rc)
 
 
 def ep_dispatch_fp8(shape: EpShape, x, x_scales, topk_idx, topk_w, send_pos, recv_base, recv_x,
-                    recv_x_scales, recv_topk_idx, recv_topk_w, recv_src_info, status, stream=None) -> None:
+                    recv_x_scales, recv_topk_idx, recv_topk_w, recv_src_info, status, stream=None,
+                    sched=None) -> None:
     """FP8 rows (uint8 e4m3 bytes, H per token) plus per-token fp32 scales
-    ([..., num_scales]; None for none).  Top-k and source info as in ep_dispatch."""
+    ([..., num_scales]; None for none).  Top-k, source info and ``sched`` as in
+    ep_dispatch."""
     R, T, K, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.hidden
     cap = _rows(recv_x, "recv_x")
     S = 0 if x_scales is None else x_scales.shape[-1]
@@ -359,7 +367,7 @@ def ep_dispatch_fp8(shape: EpShape, x, x_scales, topk_idx, topk_w, send_pos, rec
         _t(recv_topk_idx, torch.int64, (cap, K), "recv_topk_idx", nullable=True),
         _t(recv_topk_w, torch.float32, (cap, K), "recv_topk_w", nullable=True),
         _t(recv_src_info, torch.int32, (cap, 2), "recv_src_info", nullable=True),
-        _t(status, torch.int32, (1,), "status"), _stream(stream))
+        _t(status, torch.int32, (1,), "status"), _sched(sched), _stream(stream))
     _check("ep_dispatch_fp8", rc)
 
 
@@ -393,7 +401,7 @@ def ep_ll_layout(shape: EpShape, topk_idx, num_tokens_per_expert, expert_capacit
 
 
 def ep_ll_dispatch(shape: EpShape, x, topk_idx, slot_pos, expert_capacity: int, recv_x, recv_src_info,
-                   status, stream=None) -> None:
+                   status, stream=None, sched=None) -> None:
     R, T, K, E, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.num_experts, shape.hidden
     cap = expert_capacity
     rc = lib().ep_ll_dispatch(
@@ -401,7 +409,7 @@ def ep_ll_dispatch(shape: EpShape, x, topk_idx, slot_pos, expert_capacity: int, 
         _t(topk_idx, torch.int64, (R, T, K), "topk_idx"), _t(slot_pos, torch.int32, (R, T, K), "slot_pos"),
         _i32(cap), _t(recv_x, torch.bfloat16, (E, cap, H), "recv_x"),
         _t(recv_src_info, torch.int32, (E, cap, 2), "recv_src_info", nullable=True),
-        _t(status, torch.int32, (1,), "status"), _stream(stream))
+        _t(status, torch.int32, (1,), "status"), _sched(sched), _stream(stream))
     _check("ep_ll_dispatch", rc)
 
 
@@ -465,6 +473,8 @@ class Pipeline:
 
     def __post_init__(self):
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        # dispatch's unit counter: zeroed once here, every call leaves it zero
+        self.sched = torch.zeros(1, dtype=torch.int64, device=self.device)
         self.layout = alloc_layout(self.shape, self.device)
         self.notify = alloc_notify(self.shape, self.device)
         self.dispatch = alloc_dispatch(self.shape, self.capacity_rows, self.device)
@@ -474,7 +484,7 @@ class Pipeline:
         sh, L, Nt, D, C = self.shape, self.layout, self.notify, self.dispatch, self.combine
         ep_layout_notify(sh, topk_idx, L, Nt, Nt["workspace"], self.status, host_num_recv_tokens, stream)
         ep_dispatch(sh, x, topk_idx, topk_w, Nt["send_pos"], Nt["recv_base"], D["recv_x"],
-                    D["recv_topk_idx"], D["recv_topk_w"], D["recv_src_info"], self.status, stream)
+                    D["recv_topk_idx"], D["recv_topk_w"], D["recv_src_info"], self.status, stream, self.sched)
         ep_combine(sh, D["recv_x"] if y is None else y, D["recv_topk_w"] if y_w is None else y_w,
                    Nt["send_pos"], Nt["recv_base"], C["combined_x"], C["combined_w"], self.status,
                    stream)
@@ -486,7 +496,7 @@ class Pipeline:
         combined weights are not produced."""
         sh, Nt, D, C = self.shape, self.notify, self.dispatch, self.combine
         ep_dispatch(sh, x, None, None, Nt["send_pos"], Nt["recv_base"], D["recv_x"], None, None, None,
-                    self.status, stream)
+                    self.status, stream, self.sched)
         ep_combine(sh, D["recv_x"] if y is None else y, None, Nt["send_pos"], Nt["recv_base"],
                    C["combined_x"], None, self.status, stream)
         return C["combined_x"]

@@ -289,6 +289,16 @@ ep_status_t ep_notify_dispatch_noalloc(
  *   recv_topk_w    out fp32 [capacity_rows][K]   the slot's weight where its
  *                      expert lives on r, else 0
  *   recv_src_info  out int32 [capacity_rows][2]  (source rank, source token)
+ *   sched          optional (may be NULL): one device uint64, zero before
+ *                  the first call (e.g. one cudaMemset), left zero by every
+ *                  call.  Given, the CTAs take row parts from it as a counter
+ *                  once their first ring-full is done, so CTAs on SMs that
+ *                  write faster take more (the pages' static split leaves
+ *                  the whole call waiting on the slowest SM); NULL keeps the
+ *                  static split, and so does a call whose CTAs have no more
+ *                  row parts than their ring holds (small calls).  Calls whose executions may overlap on the
+ *                  GPU (different streams, concurrent host threads) need one
+ *                  sched word each.  Results are the same either way.
  * Rows beyond recv_base[R] are left untouched.
  * Cached mode ([RT] intranodeDispatch / internodeDispatch with cachedMode,
  * where the top-k is not dispatched): a handle (send_pos, recv_base) from an
@@ -306,7 +316,7 @@ ep_status_t ep_notify_dispatch_noalloc(
 ep_status_t ep_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
                         const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
                         int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
-                        float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                        float* recv_topk_w, int32_t* recv_src_info, int32_t* status, uint64_t* sched,
                         cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -330,7 +340,7 @@ ep_status_t ep_dispatch_fp8(const ep_shape_t* shape, const uint8_t* x, const flo
                             const int32_t* send_pos, const int64_t* recv_base, int64_t capacity_rows,
                             uint8_t* recv_x, float* recv_x_scales, int64_t* recv_topk_idx,
                             float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                            cudaStream_t stream);
+                            uint64_t* sched, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Step 4 - combine.  [RT] intranodeCombine / internodeCombine (combined_x is
@@ -395,7 +405,7 @@ ep_status_t ep_combine(const ep_shape_t* shape, const uint16_t* y, const float* 
  *                                                source rank in the buffer
  *   count                  out int32 [E]        rows in each buffer (before
  *                                                any capacity drop)
- * ep_ll_dispatch
+ * ep_ll_dispatch (sched as for ep_dispatch)
  *   x [R][T][H] bf16, topk_idx, slot_pos (from ep_ll_layout) ->
  *   recv_x [E][expert_capacity][H] bf16, recv_src_info [E][expert_capacity][2]
  *   (source rank, token; may be NULL).  Rows not written are left as they are.
@@ -409,7 +419,8 @@ ep_status_t ep_ll_layout(const ep_shape_t* shape, const int64_t* topk_idx,
                          cudaStream_t stream);
 ep_status_t ep_ll_dispatch(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
                            const int32_t* slot_pos, int32_t expert_capacity, uint16_t* recv_x,
-                           int32_t* recv_src_info, int32_t* status, cudaStream_t stream);
+                           int32_t* recv_src_info, int32_t* status, uint64_t* sched,
+                           cudaStream_t stream);
 ep_status_t ep_ll_combine(const ep_shape_t* shape, const uint16_t* y, int32_t expert_capacity,
                           const int64_t* topk_idx, const float* topk_w, const int32_t* slot_pos,
                           uint16_t* combined_x, int32_t* status, cudaStream_t stream);
@@ -444,7 +455,9 @@ ep_status_t ep_debug_notify_dispatch_stall(
 
 /* ------------------------------------------------------------------------
  * Testing hook for failure detection in dispatch.  Runs ep_dispatch (same
- * arguments) with CTA `stall_cta` withholding every ring-slot release and
+ * arguments) with CTA `stall_cta` withholding every ring-slot release (with
+ * `sched` given, that CTA then keeps taking units from the counter, leaving
+ * them undone, until it runs dry, so the word still ends at zero) and
  * every device wait bounded by `wait_limit_us` microseconds (1 .. 2e6).  That
  * CTA's producer gives up waiting for a free slot, its storer gives up
  * waiting for the next unit, both set EP_DEV_TIMEOUT and the CTA exits after
@@ -457,7 +470,8 @@ ep_status_t ep_debug_dispatch_stall(const ep_shape_t* shape, const uint16_t* x, 
                                     const float* topk_w, const int32_t* send_pos, const int64_t* recv_base,
                                     int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
                                     float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
-                                    int32_t stall_cta, int32_t wait_limit_us, cudaStream_t stream);
+                                    uint64_t* sched, int32_t stall_cta, int32_t wait_limit_us,
+                                    cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -108,15 +108,19 @@ def test_invalid_calls_return_before_touching_the_device(ep):
                                     vp(0)) == ep.EP_ERR_INVALID_ARG
     assert L.ep_get_dispatch_layout(ctypes.byref(good), vp(None), fake, fake, fake, fake, fake,
                                     vp(0)) == ep.EP_ERR_INVALID_ARG
+    nul = vp(None)  # sched: optional
     assert L.ep_dispatch(ctypes.byref(good), fake, fake, fake, fake, fake, ctypes.c_int64(-1), fake,
-                         fake, fake, fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
+                         fake, fake, fake, fake, nul, vp(0)) == ep.EP_ERR_INVALID_ARG
     assert L.ep_dispatch(ctypes.byref(good), odd, fake, fake, fake, fake, ctypes.c_int64(8), fake,
-                         fake, fake, fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
+                         fake, fake, fake, fake, nul, vp(0)) == ep.EP_ERR_INVALID_ARG
     # top-k arrays are all-or-none (none = cached mode)
     assert L.ep_dispatch(ctypes.byref(good), fake, fake, vp(None), fake, fake, ctypes.c_int64(8), fake,
-                         fake, fake, fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
+                         fake, fake, fake, fake, nul, vp(0)) == ep.EP_ERR_INVALID_ARG
     assert L.ep_dispatch(ctypes.byref(good), fake, fake, fake, fake, fake, ctypes.c_int64(8), fake,
-                         vp(None), vp(None), fake, fake, vp(0)) == ep.EP_ERR_INVALID_ARG
+                         vp(None), vp(None), fake, fake, nul, vp(0)) == ep.EP_ERR_INVALID_ARG
+    # a misaligned sched word is refused
+    assert L.ep_dispatch(ctypes.byref(good), fake, fake, fake, fake, fake, ctypes.c_int64(8), fake,
+                         fake, fake, fake, fake, odd, vp(0)) == ep.EP_ERR_INVALID_ARG
     assert L.ep_combine(ctypes.byref(good), vp(None), vp(None), 4, fake, fake, fake, vp(None), fake,
                         vp(0)) == ep.EP_ERR_INVALID_ARG  # y missing
     assert L.ep_combine(ctypes.byref(good), fake, vp(None), 4, fake, fake, fake, fake, fake,

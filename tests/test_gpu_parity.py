@@ -250,7 +250,8 @@ def test_stalled_lookback_times_out_and_context_survives():
     full_parity(CONFIGS["tiny"], random_expert=False)
 
 
-def test_stalled_dispatch_times_out_and_context_survives():
+@pytest.mark.parametrize("dynamic", [False, True], ids=["static", "dynamic"])
+def test_stalled_dispatch_times_out_and_context_survives(dynamic):
     """A dispatch CTA whose storer never frees a ring slot: its producer's and
     storer's bounded waits run out, the status word reports EP_ERR_TIMEOUT, the
     other CTAs finish, and the next normal dispatch on the same buffers is
@@ -267,17 +268,51 @@ def test_stalled_dispatch_times_out_and_context_survives():
     sp, rb = torch.from_numpy(nt_ref["send_pos"]).cuda(), torch.from_numpy(nt_ref["recv_base"]).cuda()
     D = ep.alloc_dispatch(sh, rows)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sched = torch.zeros(1, dtype=torch.int64, device="cuda") if dynamic else None
     ep.ep_debug_dispatch_stall(sh, x.cuda(), idx.cuda(), wt.cuda(), sp, rb, D["recv_x"], D["recv_topk_idx"],
-                               D["recv_topk_w"], D["recv_src_info"], status, stall_cta=0, wait_limit_us=2000)
+                               D["recv_topk_w"], D["recv_src_info"], status, stall_cta=0, wait_limit_us=2000,
+                               sched=sched)
     assert ep.ep_sync_status(status) == ep.EP_ERR_TIMEOUT
+    if dynamic:  # the stalled CTA took the rest of the units and the counter still ended at zero
+        assert int(sched.item()) == 0
     status.zero_()
     ep.ep_dispatch(sh, x.cuda(), idx.cuda(), wt.cuda(), sp, rb, D["recv_x"], D["recv_topk_idx"], D["recv_topk_w"],
-                   D["recv_src_info"], status)
+                   D["recv_src_info"], status, sched=sched)
     assert ep.ep_sync_status(status) == ep.EP_OK
     dp = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, x.view(torch.int16).numpy().view(np.uint16), idx.numpy(),
                     wt.numpy(), nt_ref["send_pos"], nt_ref["recv_base"])
     assert_equal("recv_x after a stalled run", u16(D["recv_x"]), dp["recv_x"])
     assert_equal("recv_src_info after a stalled run", D["recv_src_info"].cpu().numpy(), dp["recv_src_info"])
+
+
+@pytest.mark.parametrize("name", ["prefill_like", "fp8_rows_like", "tiny"])
+def test_dispatch_dynamic_assignment_matches_oracle(name):
+    """Row parts handed out through the sched counter: bit-exact, whatever CTA
+    takes which unit, and the counter is back at zero after every call."""
+    w = {"prefill_like": Workload("e", R=8, T=1024, H=7168, E=64, K=8, C=6),
+         "fp8_rows_like": Workload("e", R=16, T=512, H=2048, E=128, K=6, C=4, routing="zipf"),
+         "tiny": CONFIGS["tiny"]}[name]
+    idx, wt, x = make_inputs(w)
+    o = oracle.load()
+    lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+    nt_ref = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref)
+    dp = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, x.view(torch.int16).numpy().view(np.uint16), idx.numpy(),
+                    wt.numpy(), nt_ref["send_pos"], nt_ref["recv_base"])
+    rows = int(nt_ref["recv_base"][-1])
+    sh = shape_of(w)
+    sp, rb = torch.from_numpy(nt_ref["send_pos"]).cuda(), torch.from_numpy(nt_ref["recv_base"]).cuda()
+    sched = torch.zeros(1, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        D = ep.alloc_dispatch(sh, max(rows, 1))
+        ep.ep_dispatch(sh, x.cuda(), idx.cuda(), wt.cuda(), sp, rb, D["recv_x"], D["recv_topk_idx"],
+                       D["recv_topk_w"], D["recv_src_info"], status, sched=sched)
+        assert ep.ep_sync_status(status) == ep.EP_OK
+        assert int(sched.item()) == 0
+        assert_equal("recv_x (dynamic)", u16(D["recv_x"][:rows]), dp["recv_x"])
+        assert_equal("recv_topk_idx (dynamic)", D["recv_topk_idx"][:rows].cpu().numpy(), dp["recv_topk_idx"])
+        assert_equal("recv_topk_w (dynamic)", D["recv_topk_w"][:rows].cpu().numpy(), dp["recv_topk_w"])
+        assert_equal("recv_src_info (dynamic)", D["recv_src_info"][:rows].cpu().numpy(), dp["recv_src_info"])
 
 
 def test_invalid_arguments_rejected_on_host():
@@ -423,9 +458,11 @@ def test_dispatch_fp8_matches_oracle(name, cached):
     rti = None if cached else torch.empty(cap, w.K, dtype=torch.int64, device="cuda")
     rtw = None if cached else torch.empty(cap, w.K, dtype=torch.float32, device="cuda")
     rsi = torch.empty(cap, 2, dtype=torch.int32, device="cuda")
+    sched = None if cached else torch.zeros(1, dtype=torch.int64, device="cuda")  # dynamic / static split
     ep.ep_dispatch_fp8(sh, xb.cuda(), xs.cuda(), None if cached else idx.cuda(), None if cached else wt.cuda(),
-                       nt["send_pos"], nt["recv_base"], rx, rs, rti, rtw, rsi, status)
+                       nt["send_pos"], nt["recv_base"], rx, rs, rti, rtw, rsi, status, sched=sched)
     assert ep.ep_sync_status(status) == ep.EP_OK
+    assert sched is None or int(sched.item()) == 0
     lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
     nt_ref = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref)
     ref = o.dispatch_fp8(w.R, w.T, w.K, w.E, w.H, w.C, xb.numpy(), xs.numpy(), idx.numpy(), wt.numpy(),
@@ -462,7 +499,8 @@ def _ll_run(w, cap, idx, wt, x, y=None):
     ep.ep_ll_layout(sh, idx.cuda(), lay["num_tokens_per_expert"], cap, slot, rng_, cnt, status)
     rx = torch.zeros(w.E, cap, w.H, dtype=torch.bfloat16, device="cuda")
     src = torch.full((w.E, cap, 2), -1, dtype=torch.int32, device="cuda")
-    ep.ep_ll_dispatch(sh, x, idx.cuda(), slot, cap, rx, src, status)
+    sched = torch.zeros(1, dtype=torch.int64, device="cuda")
+    ep.ep_ll_dispatch(sh, x, idx.cuda(), slot, cap, rx, src, status, sched=sched)
     out = torch.empty(w.R, w.T, w.H, dtype=torch.bfloat16, device="cuda")
     ep.ep_ll_combine(sh, rx if y is None else y, cap, idx.cuda(), wt.cuda(), slot, out, status)
     return status, slot, rng_, cnt, rx, src, out
