@@ -102,9 +102,25 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+def code_text(src: str) -> str:
+    """A CUDA/C++ source without its comments and blank lines, so that edits to
+    comments alone keep the digest below (and the ncu figures tied to it)."""
+    import re
+
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = []
+    for line in src.splitlines():
+        code = re.sub(r"//.*$", "", line).rstrip()
+        if code.strip():
+            lines.append(code)
+    return "\n".join(lines)
+
+
 def source_digest(rel: str) -> str:
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the SHA-256 of a kernel source's code (comments and
+    blank lines left out)."""
+    with open(os.path.join(ROOT, rel)) as f:
+        return hashlib.sha256(code_text(f.read()).encode()).hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):

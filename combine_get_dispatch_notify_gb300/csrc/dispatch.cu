@@ -2,9 +2,12 @@
 // SrcInfo).  Token (s,t) goes to pool row recv_base[r] + send_pos[s][t][r]
 // of every rank r it is routed to.
 //
-// Persistent CTAs walk work units (token, row part) with a stride of the
-// grid.  Each CTA runs a shared-memory ring of `slots` buffers fed by the TMA
-// engine (bulk, non-tensor copies):
+// Persistent CTAs (2 per SM, 3 for rows of 8 KB or less) walk work units
+// (token, row part): with a stride of the grid, or - when the caller passes a
+// `sched` counter and CTAs have more units than ring slots - the first
+// ring-full with that stride and every later unit from the counter, so CTAs
+// on SMs that write faster take more.  Each CTA runs a shared-memory ring of
+// `slots` buffers fed by the TMA engine (bulk, non-tensor copies):
 //   warp 0 (producer): issues the bulk global->shared copies of its first
 //        ring-full of row parts before waiting on notify (x is an input, so
 //        at small sizes all of x is in shared memory by the time the row map
@@ -21,7 +24,8 @@
 //   warps 2-3 (metadata): write recv_topk_idx / recv_topk_w / recv_src_info
 //        for the destination rows of each token with plain stores.
 // Each row is read from HBM once and written once per destination; no
-// atomics decide placement (send_pos is precomputed by notify).  Every wait
+// atomics decide placement (send_pos is precomputed by notify; the counter
+// only decides which CTA copies a unit, so results do not depend on it).  Every wait
 // is bounded; a wait that runs out sets EP_DEV_TIMEOUT and the CTA drains its
 // in-flight copies before exiting.
 #include "ep_device.cuh"

@@ -39,3 +39,14 @@ def test_reference_arm_prints_the_contract_line():
     assert set(cb["per_op_ms"]) == {"layout", "notify", "dispatch", "combine"}
     assert cb["host"]["nproc"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_kernel_digest_ignores_comments_only():
+    """The digest tying committed ncu traffic to a kernel source changes with the
+    code, not with its comments or blank lines."""
+    import bench
+    a = "int f(int x) {\n    return x + 1;  // one more\n}\n"
+    b = "// f: one more than x\nint f(int x) {\n\n    return x + 1;\n}\n/* end */\n"
+    c = "int f(int x) {\n    return x + 2;\n}\n"
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(a) != bench.code_text(c)
