@@ -234,6 +234,7 @@ def sum_over_ranks(dist, value: float) -> float:
 def host_cpu() -> dict:
     """Host cores and CPU model (the oracle runs single-threaded on one of them)."""
     model = None
+    arm = {}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
@@ -241,8 +242,12 @@ def host_cpu() -> dict:
                 if key in ("model name", "cpu model", "hardware") and ":" in line:
                     model = line.split(":", 1)[1].strip()
                     break
+                if key in ("cpu implementer", "cpu part") and ":" in line:
+                    arm.setdefault(key, line.split(":", 1)[1].strip())
     except OSError:
         pass
+    if model is None and arm:  # Arm cores list implementer and part codes instead of a name
+        model = "Arm implementer {} part {}".format(arm.get("cpu implementer", "?"), arm.get("cpu part", "?"))
     import platform
 
     return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine()}
