@@ -315,6 +315,40 @@ def test_dispatch_dynamic_assignment_matches_oracle(name):
         assert_equal("recv_src_info (dynamic)", D["recv_src_info"][:rows].cpu().numpy(), dp["recv_src_info"])
 
 
+def test_dispatch_concurrent_streams_with_own_sched_words():
+    """Two dispatch calls running at the same time on two streams, each with its
+    own sched word: both bit-exact, both words back at zero."""
+    w = Workload("e", R=8, T=1024, H=4096, E=64, K=8, C=6)
+    o = oracle.load()
+    sh = shape_of(w)
+    runs = []
+    for seed in (21, 22):
+        ws = Workload(w.name, R=w.R, T=w.T, H=w.H, E=w.E, K=w.K, C=w.C, seed=seed)
+        idx, wt, x = make_inputs(ws)
+        lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+        nt_ref = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref)
+        rows = int(nt_ref["recv_base"][-1])
+        dp = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, x.view(torch.int16).numpy().view(np.uint16), idx.numpy(),
+                        wt.numpy(), nt_ref["send_pos"], nt_ref["recv_base"])
+        dev = dict(x=x.cuda(), idx=idx.cuda(), wt=wt.cuda(), sp=torch.from_numpy(nt_ref["send_pos"]).cuda(),
+                   rb=torch.from_numpy(nt_ref["recv_base"]).cuda(), D=ep.alloc_dispatch(sh, rows),
+                   st=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                   sched=torch.zeros(1, dtype=torch.int64, device="cuda"), stream=torch.cuda.Stream())
+        runs.append((dev, dp, rows))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for dev, _, _ in runs:
+            D = dev["D"]
+            ep.ep_dispatch(sh, dev["x"], dev["idx"], dev["wt"], dev["sp"], dev["rb"], D["recv_x"], D["recv_topk_idx"],
+                           D["recv_topk_w"], D["recv_src_info"], dev["st"], stream=dev["stream"], sched=dev["sched"])
+    torch.cuda.synchronize()
+    for dev, dp, rows in runs:
+        assert ep.ep_sync_status(dev["st"]) == ep.EP_OK
+        assert int(dev["sched"].item()) == 0
+        assert_equal("recv_x (concurrent)", u16(dev["D"]["recv_x"][:rows]), dp["recv_x"])
+        assert_equal("recv_src_info (concurrent)", dev["D"]["recv_src_info"][:rows].cpu().numpy(), dp["recv_src_info"])
+
+
 def test_invalid_arguments_rejected_on_host():
     w = CONFIGS["tiny"]
     idx, wt, x = make_inputs(w)
