@@ -139,3 +139,41 @@ def test_binding_refuses_cpu_tensors(ep):
     t = torch.zeros(2, 4, 2, dtype=torch.int64)
     with pytest.raises(ValueError):
         ep.ep_get_dispatch_layout(s, t, None, None, None, None, None)
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include "ep.h"
+
+int main(void) {
+    ep_shape_t ok = {16, 128, 8, 256, 7168, 8, 1};
+    ep_shape_t bad = {12, 128, 8, 256, 7168, 8, 1};  /* 12 ranks: not a multiple of 8 */
+    printf("%d %d %d %zu %s\n", (int)ep_check_shape(&ok), (int)ep_check_shape(&bad), (int)ep_num_nodes(&ok),
+           ep_notify_workspace_bytes(&ok), ep_status_string(EP_ERR_CAPACITY));
+    return 0;
+}
+"""
+
+
+def test_c_consumer_compiles_links_and_runs(ep, tmp_path):
+    """A plain C11 program includes ep.h, links libep_gb300.so and calls its
+    host-only entry points (no device work)."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    lib_dir = os.path.dirname(ep.LIB_PATH)
+    cmd = [gcc, "-std=c11", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+           str(src), "-o", str(exe), "-L", lib_dir, "-lep_gb300", f"-Wl,-rpath,{lib_dir}"]
+    import subprocess
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    ok, bad, nodes, ws, msg = out.stdout.split(" ", 4)
+    assert int(ok) == ep.EP_OK and int(bad) == ep.EP_ERR_INVALID_ARG and int(nodes) == 2
+    assert int(ws) == 256 + 16 * 8 * (16 + 2) * 8
+    assert msg.strip() == "receive capacity exceeded"
