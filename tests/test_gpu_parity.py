@@ -349,6 +349,68 @@ def test_dispatch_concurrent_streams_with_own_sched_words():
         assert_equal("recv_src_info (concurrent)", dev["D"]["recv_src_info"][:rows].cpu().numpy(), dp["recv_src_info"])
 
 
+def test_sched_word_stays_consistent_over_a_mixed_sequence():
+    """One sched word shared by a long sequence of calls of different shapes and
+    kinds (bf16, FP8, low-latency layout; small calls that keep the static split,
+    large ones that use the counter; calls that time out on purpose): it reads
+    zero after every call, and a final call is bit-exact."""
+    o = oracle.load()
+    sched = torch.zeros(1, dtype=torch.int64, device="cuda")
+    rng = np.random.default_rng(11)
+    shapes = [Workload("e", R=8, T=1024, H=4096, E=64, K=8, C=4), Workload("e", R=16, T=64, H=512, E=32, K=4, C=2),
+              Workload("e", R=4, T=2048, H=1024, E=16, K=2, C=3, routing="zipf")]
+    prepared = []
+    for w in shapes:
+        idx, wt, x = make_inputs(w)
+        lay_ref = o.layout(w.R, w.T, w.K, w.E, idx.numpy())
+        nt_ref = o.notify(w.R, w.T, w.E, w.C, w.expert_alignment, lay_ref)
+        rows = int(nt_ref["recv_base"][-1])
+        prepared.append((w, idx, wt, x, nt_ref, rows))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for step in range(40):
+        w, idx, wt, x, nt_ref, rows = prepared[int(rng.integers(len(prepared)))]
+        sh = shape_of(w)
+        sp, rb = torch.from_numpy(nt_ref["send_pos"]).cuda(), torch.from_numpy(nt_ref["recv_base"]).cuda()
+        D = ep.alloc_dispatch(sh, rows)
+        kind = int(rng.integers(4))
+        status.zero_()
+        if kind == 0:
+            ep.ep_dispatch(sh, x.cuda(), idx.cuda(), wt.cuda(), sp, rb, D["recv_x"], D["recv_topk_idx"],
+                           D["recv_topk_w"], D["recv_src_info"], status, sched=sched)
+            assert ep.ep_sync_status(status) == ep.EP_OK
+        elif kind == 1:
+            x8 = torch.randint(0, 256, (w.R, w.T, w.H), dtype=torch.uint8, device="cuda")
+            r8 = torch.empty(rows, w.H, dtype=torch.uint8, device="cuda")
+            ep.ep_dispatch_fp8(sh, x8, None, idx.cuda(), wt.cuda(), sp, rb, r8, None, D["recv_topk_idx"],
+                               D["recv_topk_w"], D["recv_src_info"], status, sched=sched)
+            assert ep.ep_sync_status(status) == ep.EP_OK
+        elif kind == 2:
+            cap = w.R * w.T
+            slot = torch.empty(w.R, w.T, w.K, dtype=torch.int32, device="cuda")
+            ep.ep_ll_layout(sh, idx.cuda(), None, cap, slot, torch.empty(w.E, w.R, 2, dtype=torch.int32, device="cuda"),
+                            torch.empty(w.E, dtype=torch.int32, device="cuda"), status)
+            rx = torch.empty(w.E, cap, w.H, dtype=torch.bfloat16, device="cuda")
+            ep.ep_ll_dispatch(sh, x.cuda(), idx.cuda(), slot, cap, rx, None, status, sched=sched)
+            assert ep.ep_sync_status(status) == ep.EP_OK
+        else:
+            ep.ep_debug_dispatch_stall(sh, x.cuda(), idx.cuda(), wt.cuda(), sp, rb, D["recv_x"], D["recv_topk_idx"],
+                                       D["recv_topk_w"], D["recv_src_info"], status, stall_cta=1,
+                                       wait_limit_us=1000, sched=sched)
+            assert ep.ep_sync_status(status) in (ep.EP_OK, ep.EP_ERR_TIMEOUT)
+        assert int(sched.item()) == 0, f"sched not zero after call {step} (kind {kind})"
+    w, idx, wt, x, nt_ref, rows = prepared[0]
+    sh = shape_of(w)
+    D = ep.alloc_dispatch(sh, rows)
+    status.zero_()
+    ep.ep_dispatch(sh, x.cuda(), idx.cuda(), wt.cuda(), torch.from_numpy(nt_ref["send_pos"]).cuda(),
+                   torch.from_numpy(nt_ref["recv_base"]).cuda(), D["recv_x"], D["recv_topk_idx"], D["recv_topk_w"],
+                   D["recv_src_info"], status, sched=sched)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    dp = o.dispatch(w.R, w.T, w.K, w.E, w.H, w.C, x.view(torch.int16).numpy().view(np.uint16), idx.numpy(),
+                    wt.numpy(), nt_ref["send_pos"], nt_ref["recv_base"])
+    assert_equal("recv_x after the sequence", u16(D["recv_x"][:rows]), dp["recv_x"])
+
+
 def test_invalid_arguments_rejected_on_host():
     w = CONFIGS["tiny"]
     idx, wt, x = make_inputs(w)
@@ -513,6 +575,8 @@ def test_dispatch_fp8_matches_oracle(name, cached):
 # ---------------------------------------------------------------------------- low-latency layout
 LL_CASES = {
     "tiny": (CONFIGS["tiny"], 1),
+    # enough row parts per CTA that ll_dispatch takes units from the sched counter
+    "counter_sized": (Workload("e", R=8, T=2048, H=2048, E=64, K=8, C=4), 1),
     "low_latency": (CONFIGS["low_latency"], 1),
     "top1_counting_sort": (EDGE["top1_counting_sort"], 1),
     "r32_min_hidden_repeats": (EDGE["r32_min_hidden_repeats"], None),  # repeated experts: cap R*T*K
