@@ -44,7 +44,7 @@
 #define NODE_SIZE 8 /* ranks per node: NUM_MAX_NVL_PEERS, [AR] 2.2 */
 
 /* Planted mistakes.  The default build (ORACLE_MUTANT 0) has none.  The
- * tests compile copies with ORACLE_MUTANT = 1..10, each carrying one plausible
+ * tests compile copies with ORACLE_MUTANT = 1..11, each carrying one plausible
  * error, and check that the pins reject every one of them. */
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
@@ -401,8 +401,10 @@ int oracle_combine(int R, int T, int K, int H, int64_t y_rows,
             if (y_w && combined_w) {
                 for (int k = 0; k < K; ++k) {
                     float acc = 0.0f;
-                    for (int r = 0; r < R; ++r)
+                    for (int i = 0; i < R; ++i) {
+                        int r = MUT(11) ? R - 1 - i : i;
                         if (pos[r] >= 0) acc += y_w[(size_t)(recv_base[r] + pos[r]) * K + k];
+                    }
                     combined_w[((size_t)s * T + t) * K + k] = acc;
                 }
             }

@@ -337,6 +337,26 @@ def check_combine_order(o):
     assert cb["combined_x"][1, 0, 0] == 0 and cb["combined_x"][2, 0, 0] == 0  # no destination -> +0
 
 
+def check_combine_weight_order(o):
+    """The combined weights are summed in ascending rank order as well.
+
+    Token (0,0) reaches ranks 0, 1, 2 and the expert returns weight rows
+    2^24, 1, -2^24 for slot 0.  Ascending: 2^24 + 1 ties to the even 2^24,
+    minus 2^24 gives 0.  Descending: -2^24 + 1 = -16777215 (exact), plus 2^24
+    gives 1.  Slot 1 gets 1, 2^-24, -1: ascending (1 + 2^-24) rounds to 1 (a
+    tie to even), then 0; descending gives 2^-24 exactly, so any order but
+    the ascending one shows in at least one slot.
+    """
+    idx = np.array([[[0, 1, 2]], [[-1, -1, -1]], [[-1, -1, -1]]], np.int64)  # R=3, T=1, K=3, E=3
+    lay = o.layout(3, 1, 3, 3, idx)
+    nt = o.notify(3, 1, 3, 1, 1, lay)
+    y = o.f32_to_bf16(np.zeros((3, 1), np.float32))
+    yw = np.array([[2.0 ** 24, 1.0, 0.0], [1.0, 2.0 ** -24, 0.0], [-(2.0 ** 24), -1.0, 0.0]], np.float32)
+    cb = o.combine(3, 1, 3, 1, y, yw, nt["send_pos"], nt["recv_base"])
+    np.testing.assert_array_equal(cb["combined_w"][0, 0], np.array([0.0, 0.0, 0.0], np.float32))
+    assert (cb["combined_w"][1:] == 0).all()  # no destination: weights combine to +0
+
+
 def check_bf16_rounding(o):
     """The oracle's fp32 -> bf16 rounding equals torch's round-to-nearest-even."""
     rng = np.random.default_rng(3)
@@ -479,7 +499,7 @@ ALL_CHECKS = [
     check_hand_worked, check_channel_ranges_hand, check_layout_library, check_notify_library,
     check_channel_independence, check_dispatch_stable_sort, check_dispatch_counting_sort,
     check_dispatch_identity_rank, check_dispatch_topk_fields, check_combine_identity_closed_form,
-    check_combine_error_bound, check_combine_order, check_bf16_rounding, check_dispatch_cached_mode,
+    check_combine_error_bound, check_combine_order, check_combine_weight_order, check_bf16_rounding, check_dispatch_cached_mode,
     check_dispatch_fp8, check_ll_layout_library, check_ll_dispatch_and_combine,
     check_ll_combine_order_and_fma, check_ll_capacity_drop,
 ]

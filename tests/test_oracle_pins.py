@@ -23,6 +23,7 @@ MUTANTS = {
     8: "bf16 conversion truncates instead of rounding",
     9: "LL combine rounds the product before adding (no fused multiply-add)",
     10: "LL layout visits a token's slots in descending order",
+    11: "combine weights summed in descending rank order",
 }
 
 
