@@ -358,8 +358,8 @@ class Step:
         self.layout_notify_args = (self.sh, p(idx), p(La["num_tokens_per_rank"]),
                                    p(La["num_tokens_per_rdma_rank"]), p(La["num_tokens_per_expert"]),
                                    p(La["is_token_in_rank"]), *[p(Nt[k]) for k in ep._NOTIFY_OUT],
-                                   p(Nt["workspace"]), ep._sz(Nt["workspace"].numel()), st, v(None), s)
-        self.fused = ep.ep_layout_notify_fused(sh) == 1
+                                   p(pipe.ln_workspace), ep._sz(pipe.ln_workspace.numel()), st, v(None), s)
+        self.ln_form = ep.ep_layout_notify_fused(sh)
         cap = D["recv_x"].shape[0]
         sc = p(pipe.sched)
         self.dispatch_args = (self.sh, p(x), p(idx), p(wt), p(Nt["send_pos"]), p(Nt["recv_base"]),
@@ -770,10 +770,10 @@ def run_ours(args, w):
                     "sync_ms_per_step": round(e2e_sync_ms, 4),
                     "sync_value": round(total_bytes / (e2e_sync_ms * 1e-3) / 1e9, 2),
                     "result_matches_device_step": e2e_ok},
-            "gpu_launches": (3 if step.fused else 4) * args.steps,
+            "gpu_launches": 3 * args.steps,
             "launch": ("CUDA graph replay of the three C-ABI calls" if graph is not None else
                        "eager C-ABI calls") + " (ep_layout_notify " +
-                      ("as one kernel" if step.fused else "as two kernels") +
+                      ("as one cluster kernel" if step.ln_form == 1 else "as one tiled kernel") +
                       ", ep_dispatch, ep_combine); kernels chained by programmatic dependent launch",
             "ms_per_step_eager_with_op_events": round(eager_ms, 5),
             "fp8_dispatch": fp8,

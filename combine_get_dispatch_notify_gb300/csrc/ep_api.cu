@@ -116,6 +116,36 @@ bool cluster_fits(const void* kernel, int cluster, int threads, size_t smem) {
 }
 
 namespace {
+struct OccKey {
+    const void* kernel;
+    int dev, threads;
+    size_t smem;
+    int blocks;
+};
+std::mutex g_occ_mu;
+OccKey g_occ_cache[64];
+int g_occ_count = 0;
+}  // namespace
+
+int max_blocks_per_sm(const void* kernel, int threads, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    for (int i = 0; i < g_occ_count; ++i) {
+        const OccKey& k = g_occ_cache[i];
+        if (k.kernel == kernel && k.dev == dev && k.threads == threads && k.smem == smem) return k.blocks;
+    }
+    int blocks = 0;
+    if (prepare_kernel(kernel, smem, false, false) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (g_occ_count < 64) g_occ_cache[g_occ_count++] = OccKey{kernel, dev, threads, smem, blocks};
+    return blocks;
+}
+
+namespace {
 
 bool make_shape(const ep_shape_t* s, Shape* out) {
     if (s == nullptr) return false;
@@ -202,6 +232,53 @@ ep_status_t notify_common(const ep_shape_t* shape, const uint8_t* is_token_in_ra
                       stream));
 }
 
+// Pointer checks shared by the one-call layout + notify entry points; fills
+// the notify outputs of `a`.
+ep_status_t layout_notify_args(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+                               int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                               uint8_t* is_token_in_rank, int32_t* rank_prefix_matrix,
+                               int32_t* gbl_channel_prefix_matrix, int32_t* rdma_channel_prefix_matrix,
+                               int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+                               int32_t* recv_channel_offset, int32_t* num_recv_tokens,
+                               int32_t* num_rdma_recv_tokens, int32_t* num_recv_tokens_per_expert,
+                               int64_t* recv_base, int32_t* send_pos, int32_t* status,
+                               int32_t* host_num_recv_tokens, NotifyArgs* a) {
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (!array_ok(topk_idx, tokens * sh.K, 16) || !aligned4(num_tokens_per_rank) ||
+        !aligned4(num_tokens_per_rdma_rank) || !aligned4(num_tokens_per_expert) ||
+        !array_ok(is_token_in_rank, tokens * sh.R, 16) || !array_ok(send_pos, tokens * sh.R, 16) ||
+        !aligned4(status) || !aligned4(rank_prefix_matrix) || !aligned4(gbl_channel_prefix_matrix) ||
+        !aligned4(rdma_channel_prefix_matrix) || !aligned4(recv_gbl_rank_prefix_sum) ||
+        !aligned4(recv_rdma_rank_prefix_sum) || !aligned4(recv_channel_offset) || !aligned4(num_recv_tokens) ||
+        !aligned4(num_rdma_recv_tokens) || !aligned4(num_recv_tokens_per_expert) || !aligned8(recv_base))
+        return EP_ERR_INVALID_ARG;
+    if (host_num_recv_tokens != nullptr && !aligned4(host_num_recv_tokens)) return EP_ERR_INVALID_ARG;
+    a->rank_prefix_matrix = rank_prefix_matrix;
+    a->gbl_channel_prefix_matrix = gbl_channel_prefix_matrix;
+    a->rdma_channel_prefix_matrix = rdma_channel_prefix_matrix;
+    a->recv_gbl_rank_prefix_sum = recv_gbl_rank_prefix_sum;
+    a->recv_rdma_rank_prefix_sum = recv_rdma_rank_prefix_sum;
+    a->recv_channel_offset = recv_channel_offset;
+    a->num_recv_tokens = num_recv_tokens;
+    a->num_rdma_recv_tokens = num_rdma_recv_tokens;
+    a->num_recv_tokens_per_expert = num_recv_tokens_per_expert;
+    a->recv_base = recv_base;
+    a->send_pos = send_pos;
+    a->status = status;
+    a->host_num_recv_tokens = host_num_recv_tokens;
+    return EP_OK;
+}
+
+// Which kernel ep_layout_notify runs: 1 = one thread-block cluster of R CTAs
+// (small sources: R <= 16, R * T <= kClusterMaxTokens, the cluster fits),
+// 2 = the tiled form (any shape).
+constexpr long long kClusterMaxTokens = 4096;
+
+int layout_notify_form(const Shape& sh) {
+    if (static_cast<long long>(sh.R) * sh.T <= kClusterMaxTokens && layout_notify_fused_ok(sh)) return 1;
+    return 2;
+}
+
 }  // namespace
 // Argument checks and launch shared by ep_dispatch and its stall test hook.
 ep_status_t dispatch_common(const ep_shape_t* shape, const uint16_t* x, const int64_t* topk_idx,
@@ -282,7 +359,13 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
 int32_t ep_layout_notify_fused(const ep_shape_t* shape) {
     ep::Shape sh;
     if (!ep::make_shape(shape, &sh)) return -1;
-    return ep::layout_notify_fused_ok(sh) ? 1 : 0;
+    return ep::layout_notify_form(sh);
+}
+
+size_t ep_layout_notify_workspace_bytes(const ep_shape_t* shape) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return 0;
+    return ep::tiled_workspace_bytes(sh, ep::tiled_tile_tokens(sh, 0));
 }
 
 ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
@@ -297,48 +380,50 @@ ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
                              int32_t* status, int32_t* host_num_recv_tokens, cudaStream_t stream) {
     ep::Shape sh;
     if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
-    const long long tokens = static_cast<long long>(sh.R) * sh.T;
-    if (!ep::array_ok(topk_idx, tokens * sh.K, 16) || !ep::aligned4(num_tokens_per_rank) ||
-        !ep::aligned4(num_tokens_per_rdma_rank) || !ep::aligned4(num_tokens_per_expert) ||
-        !ep::array_ok(is_token_in_rank, tokens * sh.R, 16) || !ep::array_ok(send_pos, tokens * sh.R, 16) ||
-        !ep::aligned4(status))
-        return EP_ERR_INVALID_ARG;
-    if (!ep::layout_notify_fused_ok(sh)) {
-        // two kernels: the layout step, then notify on its outputs
-        const ep_status_t st = ep_get_dispatch_layout(shape, topk_idx, num_tokens_per_rank,
-                                                      num_tokens_per_rdma_rank, num_tokens_per_expert,
-                                                      is_token_in_rank, status, stream);
-        if (st != EP_OK) return st;
-        return ep_notify_dispatch(shape, is_token_in_rank, num_tokens_per_rank, num_tokens_per_rdma_rank,
-                                  num_tokens_per_expert, rank_prefix_matrix, gbl_channel_prefix_matrix,
-                                  rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
-                                  recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
-                                  num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos,
-                                  workspace, workspace_bytes, status, host_num_recv_tokens, stream);
-    }
-    if (!ep::aligned4(rank_prefix_matrix) || !ep::aligned4(gbl_channel_prefix_matrix) ||
-        !ep::aligned4(rdma_channel_prefix_matrix) || !ep::aligned4(recv_gbl_rank_prefix_sum) ||
-        !ep::aligned4(recv_rdma_rank_prefix_sum) || !ep::aligned4(recv_channel_offset) ||
-        !ep::aligned4(num_recv_tokens) || !ep::aligned4(num_rdma_recv_tokens) ||
-        !ep::aligned4(num_recv_tokens_per_expert) || !ep::aligned8(recv_base))
-        return EP_ERR_INVALID_ARG;
-    if (host_num_recv_tokens != nullptr && !ep::aligned4(host_num_recv_tokens)) return EP_ERR_INVALID_ARG;
     ep::NotifyArgs a = {};
-    a.rank_prefix_matrix = rank_prefix_matrix;
-    a.gbl_channel_prefix_matrix = gbl_channel_prefix_matrix;
-    a.rdma_channel_prefix_matrix = rdma_channel_prefix_matrix;
-    a.recv_gbl_rank_prefix_sum = recv_gbl_rank_prefix_sum;
-    a.recv_rdma_rank_prefix_sum = recv_rdma_rank_prefix_sum;
-    a.recv_channel_offset = recv_channel_offset;
-    a.num_recv_tokens = num_recv_tokens;
-    a.num_rdma_recv_tokens = num_rdma_recv_tokens;
-    a.num_recv_tokens_per_expert = num_recv_tokens_per_expert;
-    a.recv_base = recv_base;
-    a.send_pos = send_pos;
-    a.status = status;
-    a.host_num_recv_tokens = host_num_recv_tokens;
-    return ep::from_cuda(ep::launch_layout_notify(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
-                                                  num_tokens_per_expert, is_token_in_rank, a, stream));
+    const ep_status_t st = ep::layout_notify_args(
+        sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank,
+        rank_prefix_matrix, gbl_channel_prefix_matrix, rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
+        recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens, num_rdma_recv_tokens,
+        num_recv_tokens_per_expert, recv_base, send_pos, status, host_num_recv_tokens, &a);
+    if (st != EP_OK) return st;
+    const int TT = ep::tiled_tile_tokens(sh, 0);
+    if (!ep::aligned16(workspace) || workspace_bytes < ep::tiled_workspace_bytes(sh, TT)) return EP_ERR_INVALID_ARG;
+    if (ep::layout_notify_form(sh) == 1)
+        return ep::from_cuda(ep::launch_layout_notify(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                                      num_tokens_per_expert, is_token_in_rank, a, stream));
+    return ep::from_cuda(ep::launch_layout_notify_tiled(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                                        num_tokens_per_expert, is_token_in_rank, a, workspace, 0,
+                                                        -1, ep::kDefaultWaitLimitNs, stream));
+}
+
+ep_status_t ep_debug_layout_notify_tiled(
+    const ep_shape_t* shape, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+    int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+    int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix, int32_t* rdma_channel_prefix_matrix,
+    int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum, int32_t* recv_channel_offset,
+    int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens, int32_t* num_recv_tokens_per_expert,
+    int64_t* recv_base, int32_t* send_pos, void* workspace, size_t workspace_bytes, int32_t* status,
+    int32_t* host_num_recv_tokens, int32_t tile_tokens, int32_t stall_tile, int32_t wait_limit_us,
+    cudaStream_t stream) {
+    ep::Shape sh;
+    if (!ep::make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    if (tile_tokens != 0 && (tile_tokens < 32 || tile_tokens > 8192 || tile_tokens % 32 != 0))
+        return EP_ERR_INVALID_ARG;
+    if (wait_limit_us < 1 || wait_limit_us > 2000000) return EP_ERR_INVALID_ARG;
+    ep::NotifyArgs a = {};
+    const ep_status_t st = ep::layout_notify_args(
+        sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank,
+        rank_prefix_matrix, gbl_channel_prefix_matrix, rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
+        recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens, num_rdma_recv_tokens,
+        num_recv_tokens_per_expert, recv_base, send_pos, status, host_num_recv_tokens, &a);
+    if (st != EP_OK) return st;
+    const int TT = ep::tiled_tile_tokens(sh, tile_tokens);
+    if (!ep::aligned16(workspace) || workspace_bytes < ep::tiled_workspace_bytes(sh, TT)) return EP_ERR_INVALID_ARG;
+    return ep::from_cuda(ep::launch_layout_notify_tiled(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                                        num_tokens_per_expert, is_token_in_rank, a, workspace, TT,
+                                                        stall_tile, static_cast<long long>(wait_limit_us) * 1000LL,
+                                                        stream));
 }
 
 ep_status_t ep_notify_dispatch_noalloc(

@@ -66,6 +66,25 @@ cudaError_t launch_notify(const Shape& sh, const NotifyArgs& a, void* workspace,
                           bool force_lookback, int stall_block, long long wait_limit_ns,
                           cudaStream_t stream);
 
+// CTAs of `kernel` (threads, dynamic shared bytes) one SM holds at once on
+// the current device (0 on error); asked once per device and configuration.
+int max_blocks_per_sm(const void* kernel, int threads, size_t smem);
+
+// Layout and notify in one launch for any shape: the tiled form.  Tiles of
+// `tile_tokens` tokens (0: the default for the shape; else a multiple of 32,
+// at most 8192); the workspace holds tiled_workspace_bytes(sh, TT) bytes with
+// its first tiled_workspace_zero_bytes() zero before the first call (every
+// call leaves them zero).  stall_tile >= 0 (test hook): that tile never
+// publishes its lookback words.
+int tiled_tile_tokens(const Shape& sh, int requested);
+size_t tiled_workspace_bytes(const Shape& sh, int TT);
+size_t tiled_workspace_zero_bytes();
+cudaError_t launch_layout_notify_tiled(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+                                       int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                                       uint8_t* is_token_in_rank, const NotifyArgs& a, void* workspace,
+                                       int tile_tokens, int stall_tile, long long wait_limit_ns,
+                                       cudaStream_t stream);
+
 // Layout and notify in one launch (a cluster of R CTAs).  Usable when R <= 16,
 // T <= 8192 and such a cluster fits on the current device.
 bool layout_notify_fused_ok(const Shape& sh);

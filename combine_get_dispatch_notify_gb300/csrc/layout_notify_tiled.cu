@@ -1,0 +1,80 @@
+// Steps 1 and 2 in one launch for shapes of any size: the tiled form (see
+// ln_tiled.cuh).  Persistent CTAs of 256 threads take tiles of TT tokens in
+// (source rank, tile) order from a ticket; the grid is what the device holds
+// at once, at most one CTA per tile.
+#include "ln_tiled.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kTiledThreads = 256;
+constexpr long long kMaxTiles = 16384;  // the tile size grows beyond this many tiles
+
+__global__ void __launch_bounds__(kTiledThreads) layout_notify_tiled_kernel(TiledLnArgs p) {
+    extern __shared__ __align__(16) int32_t dyn[];
+    __shared__ TiledShared sh;
+    griddep_launch_dependents();
+    griddep_wait();  // top-k ids written by the preceding kernel are visible
+    const unsigned total_tickets = static_cast<unsigned>(p.n_tiles) + gridDim.x;
+    for (;;) {
+        const int b = tiled_take_ticket(p, sh, total_tickets);
+        if (b < 0) break;
+        tiled_tile(p, sh, dyn, b, sh.seq);
+    }
+}
+
+}  // namespace
+
+// Tokens per tile: 512 (fewer when T is smaller), doubled (up to 8192) while
+// there are more than kMaxTiles tiles.  The workspace is sized for this tile
+// size; the launcher may take larger tiles (fewer of them).
+int tiled_tile_tokens(const Shape& sh, int requested) {
+    if (requested > 0) return requested;
+    int TT = 512;
+    if (sh.T < TT) TT = sh.T < kWarp ? kWarp : (sh.T + kWarp - 1) / kWarp * kWarp;
+    while (TT < 8192 && static_cast<long long>(sh.R) * ((sh.T + TT - 1) / TT) > kMaxTiles) TT *= 2;
+    return TT;
+}
+
+size_t tiled_workspace_bytes(const Shape& sh, int TT) {
+    const long long tps = sh.T > 0 ? (sh.T + TT - 1) / TT : 1;
+    return tiled_workspace_layout(sh.R, sh.N, sh.R * tps).total;
+}
+
+size_t tiled_workspace_zero_bytes() { return tiled_workspace_layout(1, 1, 1).words; }
+
+size_t tiled_smem_bytes(const Shape& sh, int TT) {
+    return sizeof(int32_t) * tiled_smem_words(sh.E, TT, sh.R + sh.N);
+}
+
+cudaError_t launch_layout_notify_tiled(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+                                       int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                                       uint8_t* is_token_in_rank, const NotifyArgs& a, void* workspace,
+                                       int tile_tokens, int stall_tile, long long wait_limit_ns,
+                                       cudaStream_t stream) {
+    const void* kernel = reinterpret_cast<const void*>(layout_notify_tiled_kernel);
+    const int sms = device_sm_count();
+    int TT = tiled_tile_tokens(sh, tile_tokens);
+    if (tile_tokens == 0) {
+        // larger tiles while the tiles are more than one wave of resident CTAs
+        while (TT < 8192) {
+            const long long tiles = static_cast<long long>(sh.R) * ((sh.T + TT - 1) / TT);
+            const int per = max_blocks_per_sm(kernel, kTiledThreads, tiled_smem_bytes(sh, TT));
+            if (tiles <= static_cast<long long>(per) * sms) break;
+            TT *= 2;
+        }
+    }
+    TiledLnArgs p = tiled_args(sh, TT, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                               num_tokens_per_expert, is_token_in_rank, a, workspace);
+    p.stall_tile = stall_tile;
+    p.wait_limit_ns = wait_limit_ns;
+    const size_t smem = tiled_smem_bytes(sh, TT);
+    const int per_sm = max_blocks_per_sm(kernel, kTiledThreads, smem);
+    if (per_sm <= 0 || sms <= 0) return cudaErrorInvalidConfiguration;
+    const long long cap = static_cast<long long>(per_sm) * sms;
+    const long long grid = p.n_tiles < cap ? p.n_tiles : cap;
+    return launch_pdl(layout_notify_tiled_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTiledThreads), smem,
+                      stream, 0, false, p);
+}
+
+}  // namespace ep

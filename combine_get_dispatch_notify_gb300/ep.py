@@ -77,6 +77,9 @@ _SIGS = {
     "ep_combine": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i64] + [_vp] * 5 + [_vp]),
     "ep_layout_notify": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 + [_vp, _sz, _vp, _vp, _vp]),
     "ep_layout_notify_fused": (_i32, [ctypes.POINTER(EpShape)]),
+    "ep_layout_notify_workspace_bytes": (_sz, [ctypes.POINTER(EpShape)]),
+    "ep_debug_layout_notify_tiled": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 +
+                                     [_vp, _sz, _vp, _vp, _i32, _i32, _i32, _vp]),
     "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 15 + [_vp, _vp, _vp]),
     "ep_ll_layout": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "ep_ll_dispatch": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
@@ -234,16 +237,16 @@ def ep_notify_dispatch(shape: EpShape, is_token_in_rank, num_tokens_per_rank,
 
 
 def ep_layout_notify_fused(shape: EpShape) -> int:
-    """1 when :func:`ep_layout_notify` runs as one kernel for ``shape`` on the
-    current device, 0 when it enqueues the two separate kernels."""
+    """Which kernel :func:`ep_layout_notify` runs for ``shape`` on the current
+    device: 1 = the cluster form, 2 = the tiled form (both one launch)."""
     return int(lib().ep_layout_notify_fused(ctypes.byref(shape)))
 
 
-def ep_layout_notify(shape: EpShape, topk_idx, layout: dict, outs: dict, workspace, status,
-                     host_num_recv_tokens=None, stream=None) -> None:
-    """Layout and notify in one call.  ``layout`` holds the four layout outputs
-    (see :func:`alloc_layout`), ``outs`` the notify outputs (see
-    :func:`notify_shapes`); ``workspace`` as for :func:`ep_notify_dispatch`."""
+def ep_layout_notify_workspace_bytes(shape: EpShape) -> int:
+    return int(lib().ep_layout_notify_workspace_bytes(ctypes.byref(shape)))
+
+
+def _layout_notify_args(shape, topk_idx, layout: dict, outs: dict):
     R, T, K, E, N = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.num_experts, shape.N
     shapes = notify_shapes(shape)
     args = [_t(topk_idx, torch.int64, (R, T, K), "topk_idx"),
@@ -254,18 +257,48 @@ def ep_layout_notify(shape: EpShape, topk_idx, layout: dict, outs: dict, workspa
     for k in _NOTIFY_OUT:
         shp, dt = shapes[k]
         args.append(_t(outs[k], dt, shp, k))
-    need = ep_notify_workspace_bytes(shape)
+    return args
+
+
+def _host_counts(shape, host_num_recv_tokens) -> _vp:
+    if host_num_recv_tokens is None:
+        return _vp(None)
+    if host_num_recv_tokens.dtype != torch.int32 or host_num_recv_tokens.numel() < shape.num_ranks + 1:
+        raise ValueError("host_num_recv_tokens must be int32 with R+1 elements")
+    return _vp(host_num_recv_tokens.data_ptr())
+
+
+def _workspace(workspace, need: int, name="workspace"):
     if workspace is None or not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
-        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
-    host = _vp(None)
-    if host_num_recv_tokens is not None:
-        if host_num_recv_tokens.dtype != torch.int32 or host_num_recv_tokens.numel() < R + 1:
-            raise ValueError("host_num_recv_tokens must be int32 with R+1 elements")
-        host = _vp(host_num_recv_tokens.data_ptr())
-    rc = lib().ep_layout_notify(ctypes.byref(shape), *args, _vp(workspace.data_ptr()),
-                                _sz(workspace.numel() * workspace.element_size()),
-                                _t(status, torch.int32, (1,), "status"), host, _stream(stream))
+        raise ValueError(f"{name} must be a CUDA tensor of at least {need} bytes")
+    return _vp(workspace.data_ptr()), _sz(workspace.numel() * workspace.element_size())
+
+
+def ep_layout_notify(shape: EpShape, topk_idx, layout: dict, outs: dict, workspace, status,
+                     host_num_recv_tokens=None, stream=None) -> None:
+    """Layout and notify in one call.  ``layout`` holds the four layout outputs
+    (see :func:`alloc_layout`), ``outs`` the notify outputs (see
+    :func:`notify_shapes`); ``workspace`` from :func:`alloc_layout_notify_workspace`."""
+    args = _layout_notify_args(shape, topk_idx, layout, outs)
+    ws, nws = _workspace(workspace, ep_layout_notify_workspace_bytes(shape))
+    rc = lib().ep_layout_notify(ctypes.byref(shape), *args, ws, nws, _t(status, torch.int32, (1,), "status"),
+                                _host_counts(shape, host_num_recv_tokens), _stream(stream))
     _check("ep_layout_notify", rc)
+
+
+def ep_debug_layout_notify_tiled(shape: EpShape, topk_idx, layout: dict, outs: dict, workspace, status,
+                                 tile_tokens: int = 0, stall_tile: int = -1, wait_limit_us: int = 1000000,
+                                 host_num_recv_tokens=None, stream=None) -> None:
+    """Testing hook: :func:`ep_layout_notify` forced onto the tiled form with
+    ``tile_tokens`` tokens per tile (0: default) and optionally one tile
+    withholding its lookback words."""
+    args = _layout_notify_args(shape, topk_idx, layout, outs)
+    ws, nws = _workspace(workspace, 0)
+    rc = lib().ep_debug_layout_notify_tiled(
+        ctypes.byref(shape), *args, ws, nws, _t(status, torch.int32, (1,), "status"),
+        _host_counts(shape, host_num_recv_tokens), _i32(tile_tokens), _i32(stall_tile), _i32(wait_limit_us),
+        _stream(stream))
+    _check("ep_debug_layout_notify_tiled", rc)
 
 
 def ep_notify_dispatch_noalloc(shape: EpShape, is_token_in_rank, num_tokens_per_rank,
@@ -446,6 +479,13 @@ def alloc_notify(shape: EpShape, device="cuda") -> dict:
     return outs
 
 
+def alloc_layout_notify_workspace(shape: EpShape, device="cuda", nbytes: int | None = None) -> torch.Tensor:
+    """Zeroed workspace for :func:`ep_layout_notify` (every call leaves it ready
+    for the next one); ``nbytes`` overrides the size (e.g. for several shapes)."""
+    n = ep_layout_notify_workspace_bytes(shape) if nbytes is None else nbytes
+    return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
 def alloc_dispatch(shape: EpShape, capacity_rows: int, device="cuda") -> dict:
     H, K = shape.hidden, shape.num_topk
     return dict(recv_x=torch.empty(capacity_rows, H, dtype=torch.bfloat16, device=device),
@@ -477,12 +517,13 @@ class Pipeline:
         self.sched = torch.zeros(1, dtype=torch.int64, device=self.device)
         self.layout = alloc_layout(self.shape, self.device)
         self.notify = alloc_notify(self.shape, self.device)
+        self.ln_workspace = alloc_layout_notify_workspace(self.shape, self.device)
         self.dispatch = alloc_dispatch(self.shape, self.capacity_rows, self.device)
         self.combine = alloc_combine(self.shape, self.device)
 
     def run(self, x, topk_idx, topk_w, y=None, y_w=None, stream=None, host_num_recv_tokens=None):
         sh, L, Nt, D, C = self.shape, self.layout, self.notify, self.dispatch, self.combine
-        ep_layout_notify(sh, topk_idx, L, Nt, Nt["workspace"], self.status, host_num_recv_tokens, stream)
+        ep_layout_notify(sh, topk_idx, L, Nt, self.ln_workspace, self.status, host_num_recv_tokens, stream)
         ep_dispatch(sh, x, topk_idx, topk_w, Nt["send_pos"], Nt["recv_base"], D["recv_x"],
                     D["recv_topk_idx"], D["recv_topk_w"], D["recv_src_info"], self.status, stream, self.sched)
         ep_combine(sh, D["recv_x"] if y is None else y, D["recv_topk_w"] if y_w is None else y_w,

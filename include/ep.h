@@ -205,21 +205,37 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
  * Steps 1 and 2 in one call: ep_get_dispatch_layout followed by
  * ep_notify_dispatch on its outputs ([RT] getDispatchLayout then
  * intranode/internodeNotifyDispatch; [IN] sm0 stages 3 and 6, sm1..x stages
- * 1-3).  Every output of both calls is written, with the same values.
+ * 1-3).  Every output of both calls is written, with the same values.  Always
+ * one kernel, in one of two forms (ep_layout_notify_fused tells which):
  *
- * When R <= 16, T <= 8192 and a thread-block cluster of R CTAs fits on the
- * device, this is ONE kernel: CTA s counts source rank s's tokens and keeps
- * one ballot word per 32 tokens and destination in shared memory; after a
- * cluster barrier the cross-source sums are read from the other CTAs' shared
- * memory, so there is no workspace traffic, no wait on another launch and no
- * second pass over is_token_in_rank.  Otherwise it enqueues the two kernels
- * of the separate calls.  ep_layout_notify_fused tells which.
+ *   cluster form (R <= 16, R*T <= 4096, and a thread-block cluster of R CTAs
+ *   fits on the device): CTA s counts source rank s's tokens and keeps one
+ *   ballot word per 32 tokens and destination in shared memory; the counts
+ *   are exchanged through distributed shared memory and one cluster barrier,
+ *   so no workspace traffic and no second pass over is_token_in_rank.
+ *
+ *   tiled form (every other shape): CTAs take tiles of up to 512 tokens of
+ *   one source rank from a ticket in (source rank, tile) order ([CH]
+ *   channels are tiles of the same kind); per-rank counts pass through a
+ *   single-pass decoupled-lookback scan over all tiles ([AR] 3.2), whose
+ *   exclusive prefix is directly each tile's first row in every
+ *   destination's region; the per-source and per-rank results are computed
+ *   by the last tile of each source and the last source to finish.  A tile
+ *   waits only for tiles with smaller tickets, every wait is bounded.
  *
  * Arguments: topk_idx and the four layout outputs as for
- * ep_get_dispatch_layout; the notify outputs, workspace (used only by the
- * two-kernel form, but always required, zeroed once before first use) and
- * host_num_recv_tokens as for ep_notify_dispatch.  send_pos must be 16-byte
- * aligned.  An expert id outside [-1, E) sets EP_DEV_INPUT and is ignored.
+ * ep_get_dispatch_layout; the notify outputs and host_num_recv_tokens as for
+ * ep_notify_dispatch.  send_pos must be 16-byte aligned.  An expert id
+ * outside [-1, E) sets EP_DEV_INPUT and is ignored.
+ *   workspace        device scratch of at least
+ *                    ep_layout_notify_workspace_bytes(shape) bytes, 16-byte
+ *                    aligned, zero-filled once before its first use; every
+ *                    call leaves it ready for the next, so it is never
+ *                    cleared again.  It may serve calls of any shape in turn
+ *                    (size it for the largest), and ep_layout_notify_dispatch
+ *                    calls too, but not two calls at once, and not
+ *                    ep_notify_dispatch (whose workspace holds other data:
+ *                    zero it again before switching).
  */
 ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
                              int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank,
@@ -232,8 +248,14 @@ ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
                              int32_t* send_pos, void* workspace, size_t workspace_bytes,
                              int32_t* status, int32_t* host_num_recv_tokens, cudaStream_t stream);
 
-/* 1 when ep_layout_notify runs as one kernel for this shape on the current
- * device, 0 when it enqueues two, -1 for an invalid shape. */
+/* Bytes of workspace ep_layout_notify (and ep_layout_notify_dispatch) needs
+ * for `shape`, or 0 for an invalid shape: a 256-byte header, 1 MiB + 32 KiB
+ * of per-expert counters, 8 * (R + N) bytes per tile and 8 * R * (R + N). */
+size_t ep_layout_notify_workspace_bytes(const ep_shape_t* shape);
+
+/* Which kernel ep_layout_notify runs for this shape on the current device:
+ * 1 = the cluster form, 2 = the tiled form (both are one launch), -1 for an
+ * invalid shape. */
 int32_t ep_layout_notify_fused(const ep_shape_t* shape);
 
 /* ------------------------------------------------------------------------
@@ -253,8 +275,12 @@ int32_t ep_layout_notify_fused(const ep_shape_t* shape);
  * The call allocates and frees nothing.
  *
  * The first call on each device looks up the array's device address (a
- * cudaGetSymbolAddress with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array and
+ * cudaGetSymbolAddress with that device current) and caches it for the life
+ * of the process; make that first call before any stream capture.  The
+ * cached address belongs to the device's primary context: after
+ * cudaDeviceReset, or from another context on the same device, it no longer
+ * names the library's array, so do not use this entry point there.  All
+ * calls share the one array and
  * each clears it on `stream` before use, so two calls whose executions
  * overlap on the GPU (different streams without ordering, or concurrent
  * host threads) race on it and give undefined results; order them.
@@ -472,6 +498,27 @@ ep_status_t ep_debug_dispatch_stall(const ep_shape_t* shape, const uint16_t* x, 
                                     float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
                                     uint64_t* sched, int32_t stall_cta, int32_t wait_limit_us,
                                     cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Testing hook for the tiled form of ep_layout_notify.  Runs it whatever the
+ * shape, with tiles of `tile_tokens` tokens (0: the default; else a multiple
+ * of 32 in [32, 8192]; the workspace must then hold what that tile size
+ * needs: 256 + 1 MiB + 32 KiB + 8 * (R + N) * R * ceil(T / tile)
+ * + 8 * R * (R + N) bytes),
+ * the tile with ticket `stall_tile` (-1: none) withholding its lookback
+ * words, and every wait bounded by `wait_limit_us` microseconds (1 .. 2e6).
+ * Tiles that wait on the withheld words give up, set EP_DEV_TIMEOUT and go
+ * on, so the context stays usable; outputs are undefined after such a run.
+ */
+ep_status_t ep_debug_layout_notify_tiled(
+    const ep_shape_t* shape, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+    int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
+    int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix, int32_t* rdma_channel_prefix_matrix,
+    int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum, int32_t* recv_channel_offset,
+    int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens, int32_t* num_recv_tokens_per_expert,
+    int64_t* recv_base, int32_t* send_pos, void* workspace, size_t workspace_bytes, int32_t* status,
+    int32_t* host_num_recv_tokens, int32_t tile_tokens, int32_t stall_tile, int32_t wait_limit_us,
+    cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -1,7 +1,10 @@
 """ep_layout_notify (layout and notify in one call) vs the CPU oracle, element
-by element, through the C ABI: the one-kernel form on every shape it accepts
-(R <= 16, T <= 8192), the two-kernel form beyond, both bit-exact."""
+by element, through the C ABI: the cluster form on the shapes it takes (R <= 16,
+R*T <= 4096), the tiled form on the others, and the tiled form forced on every
+case with several tile sizes (ep_debug_layout_notify_tiled); all bit-exact."""
 from __future__ import annotations
+
+import functools
 
 import numpy as np
 import pytest
@@ -23,7 +26,7 @@ def _lib():
 
 
 def _fused_expected(w: Workload) -> int:
-    return 1 if (w.R <= 16 and w.T <= 8192) else 0
+    return 1 if (w.R <= 16 and w.R * w.T <= 4096) else 2
 
 
 def _run(w: Workload, idx: torch.Tensor, host=None):
@@ -36,7 +39,9 @@ def _run(w: Workload, idx: torch.Tensor, host=None):
         for k, v in d.items():
             if k != "workspace":
                 v.fill_(0x5A if v.dtype == torch.uint8 else -7)
-    ep.ep_layout_notify(sh, idx.cuda(), lay, nt, nt["workspace"], status, host)
+    ws = ep.alloc_layout_notify_workspace(sh)
+    ep.ep_layout_notify(sh, idx.cuda(), lay, nt, ws, status, host)
+    nt["workspace"] = ws
     return sh, lay, nt, status
 
 
@@ -51,8 +56,8 @@ CASES = {
     "tiny": CONFIGS["tiny"],
     "low_latency": CONFIGS["low_latency"],
     "prefill": CONFIGS["prefill"],
-    "skewed": CONFIGS["skewed"],  # R=16, T=8192: the largest one-kernel shape
-    "large": CONFIGS["large"],    # R=32: two kernels
+    "skewed": CONFIGS["skewed"],
+    "large": CONFIGS["large"],
     "single_rank": Workload("e", R=1, T=37, H=64, E=6, K=3, C=4, routing="replace", mask=0.2),
     "empty_tokens": Workload("e", R=4, T=0, H=64, E=8, K=2, C=3),
     "channels_exceed_tokens": Workload("e", R=8, T=50, H=128, E=64, K=4, C=64, mask=0.1),
@@ -60,7 +65,7 @@ CASES = {
     "ragged_tokens_r16": Workload("e", R=16, T=1001, H=64, E=256, K=7, C=13, routing="zipf", mask=0.05),
     "max_experts": Workload("e", R=16, T=300, H=64, E=8192, K=9, C=4, routing="replace"),
     "r5_odd_topk": Workload("e", R=5, T=257, H=64, E=40, K=5, C=9, mask=0.3),
-    "t8193_two_kernels": Workload("e", R=2, T=8193, H=64, E=16, K=2, C=3),
+    "t8193": Workload("e", R=2, T=8193, H=64, E=16, K=2, C=3),
     "r32_small": Workload("e", R=32, T=19, H=8, E=256, K=8, C=3, routing="replace", mask=0.3),
     "all_masked": Workload("e", R=8, T=40, H=64, E=16, K=4, C=4, mask=1.0),
     "k32_repeats": Workload("e", R=16, T=97, H=64, E=512, K=32, C=7, routing="replace", mask=0.1),
@@ -144,12 +149,13 @@ def test_layout_notify_first_call_inside_graph_capture():
     sh = shape_of(w)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     lay, nt = ep.alloc_layout(sh), ep.alloc_notify(sh)
+    ws = ep.alloc_layout_notify_workspace(sh)
     idx_d = idx.cuda()
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        ep.ep_layout_notify(sh, idx_d, lay, nt, nt["workspace"], status, stream=stream)
+        ep.ep_layout_notify(sh, idx_d, lay, nt, ws, status, stream=stream)
     for _ in range(2):
         for d in (lay, nt):
             for k, v in d.items():
@@ -169,7 +175,7 @@ def test_pipeline_replayed_from_a_cuda_graph(name):
     from combine_get_dispatch_notify_gb300.workloads import gen_x, worst_case_rows
 
     w = CONFIGS["low_latency"] if name == "low_latency" else Workload(
-        "e", R=32, T=24, H=256, E=256, K=8, C=3, mask=0.1)  # two-kernel layout + notify
+        "e", R=32, T=24, H=256, E=256, K=8, C=3, mask=0.1)  # tiled layout + notify
     o = oracle.load()
     sh = shape_of(w)
     pipe = ep.Pipeline(sh, max(1, worst_case_rows(w)))
@@ -207,3 +213,132 @@ def test_pipeline_replayed_from_a_cuda_graph(name):
         assert np.array_equal(pipe.dispatch["recv_src_info"][:rows].cpu().numpy(), dp["recv_src_info"])
         assert np.array_equal(cx.view(torch.int16).cpu().numpy().view(np.uint16), cb["combined_x"])
         assert np.array_equal(cw.cpu().numpy(), cb["combined_w"])
+
+
+# ----------------------------------------------------------------------------- tiled form
+def _tiled(w: Workload, idx: torch.Tensor, tile_tokens=0, ws=None, stall=-1, limit_us=1000000):
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay = ep.alloc_layout(sh)
+    nt = ep.alloc_notify(sh)
+    for d in (lay, nt):
+        for k, v in d.items():
+            if k != "workspace":
+                v.fill_(0x5A if v.dtype == torch.uint8 else -7)
+    if ws is None:
+        ws = ep.alloc_layout_notify_workspace(sh, nbytes=_tiled_ws_bytes(w, tile_tokens))
+    ep.ep_debug_layout_notify_tiled(sh, idx.cuda(), lay, nt, ws, status, tile_tokens=tile_tokens,
+                                    stall_tile=stall, wait_limit_us=limit_us)
+    return sh, lay, nt, status, ws
+
+
+def _tiled_ws_bytes(w: Workload, tile_tokens: int) -> int:
+    """Workspace the tiled form needs with tiles of ``tile_tokens`` (0: default)."""
+    sh = shape_of(w)
+    if tile_tokens == 0:
+        return ep.ep_layout_notify_workspace_bytes(sh)
+    tiles = w.R * (max(1, -(-w.T // tile_tokens)) if w.T > 0 else 1)
+    return 256 + (1 << 20) + (32 << 10) + 8 * (w.R + w.N) * tiles + 8 * w.R * (w.R + w.N)
+
+
+TILED_SIZES = (32, 96, 512, 0)
+
+
+@functools.lru_cache(maxsize=None)
+def _case_ref(name: str):
+    w = CASES[name]
+    idx, _ = gen_routing(w)
+    return idx, _oracle(w, idx)
+
+
+@pytest.mark.parametrize("tile", TILED_SIZES, ids=lambda t: f"tile{t}")
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_tiled_layout_notify_matches_oracle(name, tile):
+    w = CASES[name]
+    if tile == 32 and w.R * w.T > 200000:
+        pytest.skip("32-token tiles of a full-size workload: covered by the larger tiles")
+    idx, (lay_ref, nt_ref) = _case_ref(name)
+    sh, lay, nt, status, ws = _tiled(w, idx, tile)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    check_layout_notify(lay, nt, lay_ref, nt_ref)
+
+
+def test_tiled_workspace_serves_shapes_in_turn_and_stays_clean():
+    """One workspace, sized for the largest, serves several shapes and tile
+    sizes in turn; after every call its expert counters and per-source
+    counters are zero again."""
+    names = ["prefill", "r32_small", "ragged_tokens_r16", "empty_tokens", "prefill", "k32_repeats"]
+    need = max(_tiled_ws_bytes(CASES[n], t) for n in names for t in (32, 0))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for i, n in enumerate(names):
+        w = CASES[n]
+        tile = 32 if i % 2 else 0
+        idx, _ = gen_routing(w)
+        lay_ref, nt_ref = _oracle(w, idx)
+        sh, lay, nt, status, _ = _tiled(w, idx, tile, ws=ws)
+        assert ep.ep_sync_status(status) == ep.EP_OK
+        check_layout_notify(lay, nt, lay_ref, nt_ref)
+        head = ws[:256].cpu()
+        assert (head[8:16] == 0).all()                               # tiles arrived / finished
+        assert (head[64:192] == 0).all()                             # tiles arrived per source
+        assert int((ws[256:256 + (1 << 20) + (32 << 10)] != 0).sum()) == 0  # expert counters
+
+
+def test_tiled_stall_times_out_and_next_call_is_exact():
+    """A tile that never publishes its lookback words makes the tiles after it
+    give up (EP_ERR_TIMEOUT, no hang); a normal call afterwards is bit-exact."""
+    w = CASES["ragged_tokens_r16"]
+    idx, _ = gen_routing(w)
+    sh, lay, nt, status, ws = _tiled(w, idx, 64, stall=5, limit_us=2000)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_TIMEOUT
+    lay_ref, nt_ref = _oracle(w, idx)
+    status.zero_()
+    ep.ep_debug_layout_notify_tiled(sh, idx.cuda(), lay, nt, ws, status, tile_tokens=64)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    check_layout_notify(lay, nt, lay_ref, nt_ref)
+
+
+def test_tiled_first_call_inside_graph_capture():
+    """The tiled form's first call for a shape inside a CUDA-graph capture (its
+    occupancy query runs then); replays match the oracle."""
+    w = Workload("e", R=24, T=413, H=64, E=96, K=6, C=7, mask=0.1)
+    idx, _ = gen_routing(w)
+    lay_ref, nt_ref = _oracle(w, idx)
+    sh = shape_of(w)
+    assert ep.ep_layout_notify_fused(sh) == 2
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay, nt = ep.alloc_layout(sh), ep.alloc_notify(sh)
+    ws = ep.alloc_layout_notify_workspace(sh)
+    idx_d = idx.cuda()
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        ep.ep_layout_notify(sh, idx_d, lay, nt, ws, status, stream=stream)
+    for _ in range(3):
+        for d in (lay, nt):
+            for k, v in d.items():
+                if k != "workspace":
+                    v.fill_(-3 if v.dtype != torch.uint8 else 7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert ep.ep_sync_status(status) == ep.EP_OK
+        check_layout_notify(lay, nt, lay_ref, nt_ref)
+
+
+def test_tiled_refuses_bad_tile_sizes_and_small_workspace():
+    w = CASES["r5_odd_topk"]
+    idx, _ = gen_routing(w)
+    sh = shape_of(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay, nt = ep.alloc_layout(sh), ep.alloc_notify(sh)
+    ws = ep.alloc_layout_notify_workspace(sh)
+    for bad in (16, 48 + 1, 8224):
+        with pytest.raises(ep.EpError):
+            ep.ep_debug_layout_notify_tiled(sh, idx.cuda(), lay, nt, ws, status, tile_tokens=bad)
+    small = torch.zeros(ep.ep_layout_notify_workspace_bytes(sh) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ep.EpError):
+        ep.ep_debug_layout_notify_tiled(sh, idx.cuda(), lay, nt, small, status)
+    with pytest.raises(ValueError):
+        ep.ep_layout_notify(sh, idx.cuda(), lay, nt, small, status)
+    assert ep.ep_sync_status(status) == ep.EP_OK  # nothing was enqueued
