@@ -30,6 +30,7 @@
 // in-flight copies before exiting.
 #include "ep_device.cuh"
 #include "ep_internal.h"
+#include "ln_tiled.cuh"
 
 namespace ep {
 namespace {
@@ -72,6 +73,7 @@ struct DispatchArgs {
     long long wait_limit_ns;
     int stall_release_cta;  // test hook: this CTA's storer never frees a slot (-1: none)
     unsigned long long* sched;  // unit counter (dynamic assignment), or NULL (static)
+    int coherent;  // 1: send_pos / recv_base are written by this same launch (read through L2)
 };
 
 // Destination row this lane stands for, or -1: lane r = rank r through
@@ -92,7 +94,7 @@ __device__ __forceinline__ long long lane_row(const DispatchArgs& p, const long 
         return e * p.ll_cap + pos;
     }
     if (lane >= p.R) return -1;
-    const int32_t sp = __ldg(p.send_pos + g * p.R + lane);
+    const int32_t sp = p.coherent ? __ldcg(p.send_pos + g * p.R + lane) : __ldg(p.send_pos + g * p.R + lane);
     if (sp < 0) return -1;
     const long long row = base[lane] + sp;
     if (row >= p.capacity) {
@@ -118,61 +120,116 @@ __device__ __forceinline__ void bulk_wait_read_lag(int lag) {
     }
 }
 
-__global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int S = p.slots;
-    uint8_t* data = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * p.part_bytes);
-    uint64_t* empty = full + S;
-    SlotDesc* desc = reinterpret_cast<SlotDesc*>(empty + S);
-    long long* base = reinterpret_cast<long long*>(desc + S);
+// Shared-memory ring of one CTA and its unit schedule.
+struct Ring {
+    int S;
+    uint8_t* data;
+    uint64_t* full;
+    uint64_t* empty;
+    SlotDesc* desc;
+    long long* base;
+    bool dynamic;
+    long long P0;  // units this CTA takes with the static stride
+    int pre;       // of them, loaded before the dependency wait
+    unsigned long long dyn_units, last_grab;
+};
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    griddep_launch_dependents();
+// Bytes of the ring region (data, mbarriers, descriptors, recv_base copy).
+__host__ __device__ inline size_t ring_bytes(int slots, uint32_t part_bytes) {
+    return static_cast<size_t>(slots) * part_bytes + 2 * slots * sizeof(uint64_t) + slots * sizeof(SlotDesc) +
+           33 * sizeof(long long);
+}
+
+// Unit assignment.  Static: CTA b takes units b, b + grid, ...
+// Dynamic (counter): CTA b takes its first P0 units that way (they are the
+// ones loaded before the dependency wait), and every later unit from the
+// counter, so CTAs on faster SMs take more of them.  Each CTA's producer
+// keeps one counter grab in flight and ends on exactly one grab past the
+// end; the grab that sees the last value of the call resets the counter,
+// so every call leaves it zero for the next.
+// With fewer units per CTA than ring slots there is (almost) nothing left
+// to balance after the first ring-full, and the counter's grabs would only
+// add their latency: such calls keep the static split.
+__device__ __forceinline__ Ring ring_setup(const DispatchArgs& p, uint8_t* smem) {
+    Ring rg;
+    rg.S = p.slots;
+    rg.data = smem;
+    rg.full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(rg.S) * p.part_bytes);
+    rg.empty = rg.full + rg.S;
+    rg.desc = reinterpret_cast<SlotDesc*>(rg.empty + rg.S);
+    rg.base = reinterpret_cast<long long*>(rg.desc + rg.S);
+    const long long per_cta = p.num_units / gridDim.x;
+    rg.dynamic = p.sched != nullptr && per_cta > rg.S;
+    const long long units_here =
+        blockIdx.x < p.num_units ? (p.num_units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    rg.P0 = rg.dynamic ? (per_cta < rg.S ? per_cta : rg.S) : units_here;
+    rg.pre = static_cast<int>(rg.P0 < rg.S ? rg.P0 : rg.S);
+    rg.dyn_units = rg.dynamic ? static_cast<unsigned long long>(p.num_units - rg.P0 * gridDim.x) : 0ull;
+    rg.last_grab = rg.dyn_units + gridDim.x - 1;  // value of the call's final grab
+    return rg;
+}
+
+// mbarrier set-up, then the first ring-full of row parts: x is an input of
+// the step, not written by layout or notify, so it is loaded while the row
+// map is still being computed.
+__device__ __forceinline__ void ring_prologue(const DispatchArgs& p, const Ring& rg) {
+    const int tid = threadIdx.x;
     if (tid == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 2);  // arrivals: row part armed, descriptor written
-            mbar_init(&empty[i], 1);
+        for (int i = 0; i < rg.S; ++i) {
+            mbar_init(&rg.full[i], 2);  // arrivals: row part armed, descriptor written
+            mbar_init(&rg.empty[i], 1);
         }
         fence_mbarrier_init();
     }
     __syncthreads();
-    // x is an input of the step, not written by layout or notify, so the
-    // first ring-full of row parts is loaded while notify is still running.
-    // Unit assignment.  Static: CTA b takes units b, b + grid, ...
-    // Dynamic (counter): CTA b takes its first P0 units that way (they are the
-    // ones loaded before the dependency wait), and every later unit from the
-    // counter, so CTAs on faster SMs take more of them.  Each CTA's producer
-    // keeps one counter grab in flight and ends on exactly one grab past the
-    // end; the grab that sees the last value of the call resets the counter,
-    // so every call leaves it zero for the next.
-    // With fewer units per CTA than ring slots there is (almost) nothing left
-    // to balance after the first ring-full, and the counter's grabs would only
-    // add their latency: such calls keep the static split.
-    const long long per_cta = p.num_units / gridDim.x;
-    const bool dynamic = p.sched != nullptr && per_cta > S;
-    const long long units_here =
-        blockIdx.x < p.num_units ? (p.num_units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    const long long P0 = dynamic ? (per_cta < S ? per_cta : S) : units_here;
-    const int pre = static_cast<int>(P0 < S ? P0 : S);
-    const unsigned long long dyn_units =
-        dynamic ? static_cast<unsigned long long>(p.num_units - P0 * gridDim.x) : 0ull;
-    const unsigned long long last_grab = dyn_units + gridDim.x - 1;  // value of the call's final grab
-    if (warp == 0 && lane == 0) {
+    if (tid == 0) {
         long long u = blockIdx.x;
-        for (int i = 0; i < pre; ++i, u += gridDim.x) {
+        for (int i = 0; i < rg.pre; ++i, u += gridDim.x) {
             const long long g = u / p.parts;
             const long long off = (u - g * p.parts) * static_cast<long long>(p.part_bytes);
             const long long left = p.row_bytes - off;
             const uint32_t bytes = left < p.part_bytes ? static_cast<uint32_t>(left) : p.part_bytes;
-            mbar_arrive_expect_tx(&full[i], bytes);
-            bulk_g2s(data + static_cast<size_t>(i) * p.part_bytes, p.x + g * p.row_bytes + off, bytes,
-                     &full[i]);
+            mbar_arrive_expect_tx(&rg.full[i], bytes);
+            bulk_g2s(rg.data + static_cast<size_t>(i) * p.part_bytes, p.x + g * p.row_bytes + off, bytes,
+                     &rg.full[i]);
         }
     }
-    griddep_wait();  // send_pos / recv_base from notify are visible from here on
-    if (p.recv_base != nullptr && tid <= p.R) base[tid] = p.recv_base[tid];
-    __syncthreads();
+}
+
+// The row map never became available (a bounded wait ran out): give the
+// prefetched slots their second arrival, wait for their copies, and keep the
+// counter's grab count exact (units are left undone), then return.
+__device__ void ring_abort(const DispatchArgs& p, const Ring& rg) {
+    if (threadIdx.x != 0) return;
+    for (int i = 0; i < rg.pre; ++i) mbar_arrive(&rg.full[i]);
+    for (int i = 0; i < rg.pre; ++i)
+        if (!mbar_wait(&rg.full[i], 0, globaltimer_ns() + p.wait_limit_ns)) flag_error(p.status, EP_DEV_TIMEOUT);
+    if (rg.dynamic) {
+        unsigned long long grab = atomicAdd(p.sched, 1ull);
+        for (;;) {
+            if (grab == rg.last_grab) {
+                atomicExch(p.sched, 0ull);
+                break;
+            }
+            if (grab >= rg.dyn_units) break;
+            grab = atomicAdd(p.sched, 1ull);
+        }
+    }
+}
+
+// Producer, storer and metadata roles, once base[] holds recv_base.
+__device__ void dispatch_roles(const DispatchArgs& p, const Ring& rg) {
+    const int S = rg.S;
+    uint8_t* data = rg.data;
+    uint64_t* full = rg.full;
+    uint64_t* empty = rg.empty;
+    SlotDesc* desc = rg.desc;
+    const long long* base = rg.base;
+    const bool dynamic = rg.dynamic;
+    const long long P0 = rg.P0;
+    const int pre = rg.pre;
+    const unsigned long long dyn_units = rg.dyn_units, last_grab = rg.last_grab;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (warp == 0) {
         // ---------------- producer ----------------
@@ -368,12 +425,78 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     }
 }
 
+
+// Layout, notify and dispatch in one launch ([RT] internodeNotifyDispatch
+// followed by internodeDispatch; the pages' notify hands its results to
+// dispatch through per-channel head/tail words, here through one `ready`
+// word).  The dispatch CTAs load their first ring-full of x rows, then take
+// layout + notify tiles from the tiled form's ticket (see ln_tiled.cuh) until
+// none is left, then wait - bounded - until the call's row map is complete
+// and run the dispatch roles on it, reading send_pos and recv_base through
+// L2 since this launch wrote them.  A CTA waits only on tiles taken by CTAs
+// that are already running, so no co-residency is needed.
+__global__ void __launch_bounds__(kDispatchThreads)
+layout_notify_dispatch_kernel(DispatchArgs p, TiledLnArgs ln, uint32_t tile_smem_off) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ TiledShared sh;
+    __shared__ int s_ok;
+    griddep_launch_dependents();
+    const Ring rg = ring_setup(p, smem);
+    ring_prologue(p, rg);
+    griddep_wait();  // top-k ids written by the preceding kernel are visible
+    int32_t* dyn = reinterpret_cast<int32_t*>(smem + tile_smem_off);
+    const unsigned total_tickets = static_cast<unsigned>(ln.n_tiles) + gridDim.x;
+    for (;;) {
+        const int b = tiled_take_ticket(ln, sh, total_tickets);
+        if (b < 0) break;
+        tiled_tile(ln, sh, dyn, b, sh.seq);
+    }
+    const unsigned long long seq = sh.seq;
+    if (threadIdx.x == 0) {
+        const long long deadline = globaltimer_ns() + p.wait_limit_ns;
+        unsigned long long w = ld_acquire_u64(ln.ready);
+        uint32_t polls = 0;
+        bool ok = true;
+        while (w != seq) {
+            if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
+                ok = false;
+                break;
+            }
+            __nanosleep(64);
+            w = ld_acquire_u64(ln.ready);
+        }
+        if (!ok) flag_error(p.status, EP_DEV_TIMEOUT);
+        s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) {
+        ring_abort(p, rg);
+        return;
+    }
+    if (threadIdx.x <= p.R) rg.base[threadIdx.x] = __ldcg(p.recv_base + threadIdx.x);
+    __syncthreads();
+    dispatch_roles(p, rg);
+}
+
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    griddep_launch_dependents();
+    const Ring rg = ring_setup(p, smem);
+    ring_prologue(p, rg);
+    griddep_wait();  // send_pos / recv_base from notify are visible from here on
+    if (p.recv_base != nullptr && threadIdx.x <= p.R) rg.base[threadIdx.x] = p.recv_base[threadIdx.x];
+    __syncthreads();
+    dispatch_roles(p, rg);
+}
+
 }  // namespace
 
 namespace {
 
-// Sizes the ring for the row bytes in `p` and launches.
-cudaError_t launch_dispatch_args(DispatchArgs& p, long long tokens, cudaStream_t stream) {
+// Sizes the ring for the row bytes in `p` (leaving `extra_per_cta` shared
+// bytes per CTA for other uses) and returns the grid and dynamic shared bytes.
+cudaError_t size_dispatch(DispatchArgs& p, long long tokens, size_t extra_per_cta, long long* grid_out,
+                          size_t* smem_out) {
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const long long row_bytes = p.row_bytes;
@@ -391,15 +514,24 @@ cudaError_t launch_dispatch_args(DispatchArgs& p, long long tokens, cudaStream_t
     const long long min_units = (row_bytes <= 8192 ? 4 : 8) * grid_target;
     while (part > 2048 && units_for(part) < min_units) part = ((part / 2) + 15) / 16 * 16;
     const int parts = static_cast<int>((row_bytes + part - 1) / part);
-    int slots = static_cast<int>(kSmemPerSm / ctas_per_sm / part);
+    const long long avail = kSmemPerSm / ctas_per_sm - static_cast<long long>(extra_per_cta);
+    int slots = static_cast<int>(avail / part);
     slots = slots < 2 ? 2 : (slots > kMaxSlots ? kMaxSlots : slots);
     p.parts = parts;
     p.slots = slots;
     p.part_bytes = static_cast<uint32_t>(part);
     p.num_units = tokens * parts;
-    const size_t smem = static_cast<size_t>(slots) * part + 2 * slots * sizeof(uint64_t) +
-                        slots * sizeof(SlotDesc) + 33 * sizeof(long long);
-    const long long grid = p.num_units < grid_target ? p.num_units : grid_target;
+    *smem_out = ring_bytes(slots, p.part_bytes);
+    *grid_out = p.num_units < grid_target ? p.num_units : grid_target;
+    return cudaSuccess;
+}
+
+// Sizes the ring for the row bytes in `p` and launches.
+cudaError_t launch_dispatch_args(DispatchArgs& p, long long tokens, cudaStream_t stream) {
+    long long grid = 0;
+    size_t smem = 0;
+    const cudaError_t e = size_dispatch(p, tokens, 0, &grid, &smem);
+    if (e != cudaSuccess) return e;
     return launch_pdl(dispatch_kernel, dim3(static_cast<unsigned>(grid)), dim3(kDispatchThreads), smem,
                       stream, 0, true, p);
 }
@@ -448,6 +580,50 @@ cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, co
     p.recv_src_info = recv_src_info;
     p.row_bytes = static_cast<long long>(sh.H) * x_elem_bytes;
     return launch_dispatch_args(p, tokens, stream);
+}
+
+cudaError_t launch_layout_notify_dispatch(const Shape& sh, const int64_t* topk_idx, const float* topk_w,
+                                          const uint16_t* x, int32_t* num_tokens_per_rank,
+                                          int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                                          uint8_t* is_token_in_rank, const NotifyArgs& a, void* workspace,
+                                          int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                                          float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                                          unsigned long long* sched, int tile_tokens, int stall_tile,
+                                          long long wait_limit_ns, cudaStream_t stream) {
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    if (tokens == 0)  // nothing to dispatch: layout + notify alone
+        return launch_layout_notify_tiled(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                          num_tokens_per_expert, is_token_in_rank, a, workspace, tile_tokens,
+                                          stall_tile, wait_limit_ns, stream);
+    const int TT = tiled_tile_tokens(sh, tile_tokens);
+    TiledLnArgs ln = tiled_args(sh, TT, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                num_tokens_per_expert, is_token_in_rank, a, workspace);
+    ln.stall_tile = stall_tile;
+    ln.wait_limit_ns = wait_limit_ns;
+    ln.signal_ready = 1;
+    DispatchArgs p = base_args(sh, status);
+    p.sched = sched;
+    p.wait_limit_ns = wait_limit_ns;
+    p.coherent = 1;
+    p.x = reinterpret_cast<const uint8_t*>(x);
+    p.topk_idx = topk_w != nullptr ? topk_idx : nullptr;  // top-k fields travel only with weights
+    p.topk_w = topk_w;
+    p.send_pos = a.send_pos;
+    p.recv_base = a.recv_base;
+    p.capacity = capacity_rows;
+    p.recv_x = reinterpret_cast<uint8_t*>(recv_x);
+    p.recv_topk_idx = recv_topk_idx;
+    p.recv_topk_w = recv_topk_w;
+    p.recv_src_info = recv_src_info;
+    p.row_bytes = sh.row_bytes();
+    const size_t tile_smem = sizeof(int32_t) * tiled_smem_words(sh.E, TT, sh.R + sh.N);
+    long long grid = 0;
+    size_t ring = 0;
+    cudaError_t e = size_dispatch(p, tokens, tile_smem + sizeof(TiledShared) + 1024, &grid, &ring);
+    if (e != cudaSuccess) return e;
+    const size_t off = (ring + 15) / 16 * 16;
+    return launch_pdl(layout_notify_dispatch_kernel, dim3(static_cast<unsigned>(grid)), dim3(kDispatchThreads),
+                      off + tile_smem, stream, 0, true, p, ln, static_cast<uint32_t>(off));
 }
 
 cudaError_t launch_ll_dispatch(const Shape& sh, const uint16_t* x, const int64_t* topk_idx,

@@ -426,6 +426,96 @@ ep_status_t ep_debug_layout_notify_tiled(
                                                         stream));
 }
 
+}  // extern "C"
+
+namespace ep {
+namespace {
+
+// Argument checks and launch shared by ep_layout_notify_dispatch and its
+// stall test hook.
+ep_status_t layout_notify_dispatch_common(
+    const ep_shape_t* shape, const int64_t* topk_idx, const float* topk_w, const uint16_t* x,
+    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+    uint8_t* is_token_in_rank, int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+    int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+    int32_t* recv_channel_offset, int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+    int32_t* num_recv_tokens_per_expert, int64_t* recv_base, int32_t* send_pos, void* workspace,
+    size_t workspace_bytes, int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx, float* recv_topk_w,
+    int32_t* recv_src_info, int32_t* status, uint64_t* sched, int32_t* host_num_recv_tokens, int stall_tile,
+    long long wait_limit_ns, cudaStream_t stream) {
+    Shape sh;
+    if (!make_shape(shape, &sh)) return EP_ERR_INVALID_ARG;
+    NotifyArgs a = {};
+    const ep_status_t st = layout_notify_args(
+        sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank,
+        rank_prefix_matrix, gbl_channel_prefix_matrix, rdma_channel_prefix_matrix, recv_gbl_rank_prefix_sum,
+        recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens, num_rdma_recv_tokens,
+        num_recv_tokens_per_expert, recv_base, send_pos, status, host_num_recv_tokens, &a);
+    if (st != EP_OK) return st;
+    if (!aligned16(workspace) || workspace_bytes < tiled_workspace_bytes(sh, tiled_tile_tokens(sh, 0)))
+        return EP_ERR_INVALID_ARG;
+    if (capacity_rows < 0) return EP_ERR_INVALID_ARG;
+    const long long tokens = static_cast<long long>(sh.R) * sh.T;
+    const long long cap = capacity_rows;
+    // top-k fields: weights in, both receive arrays out - or all three NULL
+    const bool topk_given = topk_w != nullptr || recv_topk_idx != nullptr || recv_topk_w != nullptr;
+    if (topk_given && (!array_ok(topk_w, tokens * sh.K, 4) || !array_ok(recv_topk_idx, cap * sh.K, 8) ||
+                       !array_ok(recv_topk_w, cap * sh.K, 4) || (tokens > 0 && topk_w == nullptr) ||
+                       (cap > 0 && (recv_topk_idx == nullptr || recv_topk_w == nullptr))))
+        return EP_ERR_INVALID_ARG;
+    if (!array_ok(x, tokens * sh.H, 16) || !array_ok(recv_x, cap * sh.H, 16) ||
+        (recv_src_info != nullptr && !aligned8(recv_src_info)) || (sched != nullptr && !aligned8(sched)))
+        return EP_ERR_INVALID_ARG;
+    return from_cuda(launch_layout_notify_dispatch(
+        sh, topk_idx, topk_w, x, num_tokens_per_rank, num_tokens_per_rdma_rank, num_tokens_per_expert,
+        is_token_in_rank, a, workspace, capacity_rows, recv_x, recv_topk_idx, recv_topk_w, recv_src_info, status,
+        reinterpret_cast<unsigned long long*>(sched), 0, stall_tile, wait_limit_ns, stream));
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" {
+
+ep_status_t ep_layout_notify_dispatch(
+    const ep_shape_t* shape, const int64_t* topk_idx, const float* topk_w, const uint16_t* x,
+    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+    uint8_t* is_token_in_rank, int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+    int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+    int32_t* recv_channel_offset, int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+    int32_t* num_recv_tokens_per_expert, int64_t* recv_base, int32_t* send_pos, void* workspace,
+    size_t workspace_bytes, int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx, float* recv_topk_w,
+    int32_t* recv_src_info, int32_t* status, uint64_t* sched, int32_t* host_num_recv_tokens,
+    cudaStream_t stream) {
+    return ep::layout_notify_dispatch_common(
+        shape, topk_idx, topk_w, x, num_tokens_per_rank, num_tokens_per_rdma_rank, num_tokens_per_expert,
+        is_token_in_rank, rank_prefix_matrix, gbl_channel_prefix_matrix, rdma_channel_prefix_matrix,
+        recv_gbl_rank_prefix_sum, recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
+        num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos, workspace, workspace_bytes,
+        capacity_rows, recv_x, recv_topk_idx, recv_topk_w, recv_src_info, status, sched, host_num_recv_tokens, -1,
+        ep::kDefaultWaitLimitNs, stream);
+}
+
+ep_status_t ep_debug_layout_notify_dispatch_stall(
+    const ep_shape_t* shape, const int64_t* topk_idx, const float* topk_w, const uint16_t* x,
+    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+    uint8_t* is_token_in_rank, int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+    int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+    int32_t* recv_channel_offset, int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+    int32_t* num_recv_tokens_per_expert, int64_t* recv_base, int32_t* send_pos, void* workspace,
+    size_t workspace_bytes, int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx, float* recv_topk_w,
+    int32_t* recv_src_info, int32_t* status, uint64_t* sched, int32_t stall_tile, int32_t wait_limit_us,
+    cudaStream_t stream) {
+    if (stall_tile < 0 || wait_limit_us < 1 || wait_limit_us > 2000000) return EP_ERR_INVALID_ARG;
+    return ep::layout_notify_dispatch_common(
+        shape, topk_idx, topk_w, x, num_tokens_per_rank, num_tokens_per_rdma_rank, num_tokens_per_expert,
+        is_token_in_rank, rank_prefix_matrix, gbl_channel_prefix_matrix, rdma_channel_prefix_matrix,
+        recv_gbl_rank_prefix_sum, recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens,
+        num_rdma_recv_tokens, num_recv_tokens_per_expert, recv_base, send_pos, workspace, workspace_bytes,
+        capacity_rows, recv_x, recv_topk_idx, recv_topk_w, recv_src_info, status, sched, nullptr, stall_tile,
+        static_cast<long long>(wait_limit_us) * 1000LL, stream);
+}
+
 ep_status_t ep_notify_dispatch_noalloc(
     const ep_shape_t* shape, const uint8_t* is_token_in_rank, const int32_t* num_tokens_per_rank,
     const int32_t* num_tokens_per_rdma_rank, const int32_t* num_tokens_per_expert,

@@ -106,6 +106,18 @@ cudaError_t launch_dispatch(const Shape& sh, const void* x, int x_elem_bytes, co
                             unsigned long long* sched, cudaStream_t stream, int stall_release_cta = -1,
                             long long wait_limit_ns = 1000000000LL);
 
+// Layout, notify and dispatch in one launch (the tiled layout + notify inside
+// the dispatch grid; see ep_layout_notify_dispatch).  Top-k fields travel
+// when topk_w is given.
+cudaError_t launch_layout_notify_dispatch(const Shape& sh, const int64_t* topk_idx, const float* topk_w,
+                                          const uint16_t* x, int32_t* num_tokens_per_rank,
+                                          int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                                          uint8_t* is_token_in_rank, const NotifyArgs& a, void* workspace,
+                                          int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx,
+                                          float* recv_topk_w, int32_t* recv_src_info, int32_t* status,
+                                          unsigned long long* sched, int tile_tokens, int stall_tile,
+                                          long long wait_limit_ns, cudaStream_t stream);
+
 cudaError_t launch_combine(const Shape& sh, const uint16_t* y, const float* y_w, int64_t y_rows,
                            const int32_t* send_pos, const int64_t* recv_base, uint16_t* combined_x,
                            float* combined_w, int32_t* status, cudaStream_t stream);

@@ -211,7 +211,7 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
 
 // One tile b (of source b / tps).  `dyn` holds tiled_smem_words() words.
 // Every thread of the CTA calls it; blockDim.x is a multiple of 32.
-__device__ void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t* dyn, int b, unsigned seq) {
+__device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t* dyn, int b, unsigned seq) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = static_cast<int>(blockDim.x), warps = B >> 5;
     const int R = p.R, N = p.N, V = p.V, K = p.K, T = p.T, E = p.E, C = p.C;

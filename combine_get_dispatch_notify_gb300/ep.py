@@ -80,6 +80,10 @@ _SIGS = {
     "ep_layout_notify_workspace_bytes": (_sz, [ctypes.POINTER(EpShape)]),
     "ep_debug_layout_notify_tiled": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 16 +
                                      [_vp, _sz, _vp, _vp, _i32, _i32, _i32, _vp]),
+    "ep_layout_notify_dispatch": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 18 + [_vp, _sz, _i64] + [_vp] * 7 +
+                                  [_vp]),
+    "ep_debug_layout_notify_dispatch_stall": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 18 + [_vp, _sz, _i64] +
+                                              [_vp] * 6 + [_i32, _i32, _vp]),
     "ep_notify_dispatch_noalloc": (_i32, [ctypes.POINTER(EpShape)] + [_vp] * 15 + [_vp, _vp, _vp]),
     "ep_ll_layout": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "ep_ll_dispatch": (_i32, [ctypes.POINTER(EpShape), _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
@@ -335,6 +339,43 @@ def ep_debug_notify_dispatch_stall(shape: EpShape, is_token_in_rank, num_tokens_
 
 def _sched(sched):
     return _t(sched, torch.int64, (1,), "sched", nullable=True)
+
+
+def _lnd_args(shape, x, topk_idx, topk_w, layout, outs, workspace, disp, sched):
+    R, T, K, H = shape.num_ranks, shape.num_tokens, shape.num_topk, shape.hidden
+    ln = _layout_notify_args(shape, topk_idx, layout, outs)
+    cap = _rows(disp["recv_x"], "recv_x")
+    ws, nws = _workspace(workspace, ep_layout_notify_workspace_bytes(shape))
+    return ([ln[0], _t(topk_w, torch.float32, (R, T, K), "topk_w", nullable=True),
+             _t(x, torch.bfloat16, (R, T, H), "x")] + ln[1:] +
+            [ws, nws, _i64(cap), _t(disp["recv_x"], torch.bfloat16, (cap, H), "recv_x"),
+             _t(disp.get("recv_topk_idx"), torch.int64, (cap, K), "recv_topk_idx", nullable=True),
+             _t(disp.get("recv_topk_w"), torch.float32, (cap, K), "recv_topk_w", nullable=True),
+             _t(disp.get("recv_src_info"), torch.int32, (cap, 2), "recv_src_info", nullable=True)])
+
+
+def ep_layout_notify_dispatch(shape: EpShape, x, topk_idx, topk_w, layout: dict, outs: dict, workspace,
+                              disp: dict, status, sched=None, host_num_recv_tokens=None, stream=None) -> None:
+    """Layout, notify and dispatch in one launch.  ``layout``/``outs`` as for
+    :func:`ep_layout_notify`, ``disp`` holds the receive arrays (see
+    :func:`alloc_dispatch`; recv_topk_idx / recv_topk_w / recv_src_info may be
+    missing or None, and topk_w None with them)."""
+    args = _lnd_args(shape, x, topk_idx, topk_w, layout, outs, workspace, disp, sched)
+    rc = lib().ep_layout_notify_dispatch(ctypes.byref(shape), *args, _t(status, torch.int32, (1,), "status"),
+                                         _sched(sched), _host_counts(shape, host_num_recv_tokens), _stream(stream))
+    _check("ep_layout_notify_dispatch", rc)
+
+
+def ep_debug_layout_notify_dispatch_stall(shape: EpShape, x, topk_idx, topk_w, layout: dict, outs: dict,
+                                          workspace, disp: dict, status, stall_tile: int, wait_limit_us: int,
+                                          sched=None, stream=None) -> None:
+    """Testing hook: :func:`ep_layout_notify_dispatch` with one layout + notify
+    tile withholding its lookback words and every wait bounded."""
+    args = _lnd_args(shape, x, topk_idx, topk_w, layout, outs, workspace, disp, sched)
+    rc = lib().ep_debug_layout_notify_dispatch_stall(
+        ctypes.byref(shape), *args, _t(status, torch.int32, (1,), "status"), _sched(sched), _i32(stall_tile),
+        _i32(wait_limit_us), _stream(stream))
+    _check("ep_debug_layout_notify_dispatch_stall", rc)
 
 
 def ep_dispatch(shape: EpShape, x, topk_idx, topk_w, send_pos, recv_base, recv_x, recv_topk_idx,

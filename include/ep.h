@@ -369,6 +369,39 @@ ep_status_t ep_dispatch_fp8(const ep_shape_t* shape, const uint8_t* x, const flo
                             uint64_t* sched, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Steps 1 to 3 in one launch: ep_layout_notify followed by ep_dispatch on
+ * its row map ([RT] internodeNotifyDispatch then internodeDispatch; where
+ * the pages hand notify's results to dispatch through per-channel head/tail
+ * words, here one `ready` word of the workspace carries the call's sequence
+ * number).  The dispatch CTAs load their first ring-full of x rows, take
+ * tiles of the tiled layout + notify form (see ep_layout_notify) from its
+ * ticket until none is left, wait - bounded, EP_DEV_TIMEOUT - until the
+ * row map of the call is complete, and copy.  A CTA waits only on tiles taken
+ * by CTAs that are already running, so the launch needs no co-residency.
+ * Every output of ep_layout_notify and of ep_dispatch is written, with the
+ * same values as the two calls.
+ *
+ * Arguments: topk_idx, the four layout outputs, the eleven notify outputs,
+ * workspace / workspace_bytes (as for ep_layout_notify, the same workspace
+ * may serve both calls in turn) and host_num_recv_tokens as for
+ * ep_layout_notify; x, capacity_rows, recv_x, recv_src_info (may be NULL)
+ * and sched as for ep_dispatch.  topk_w, recv_topk_idx and recv_topk_w
+ * carry the top-k fields as in ep_dispatch, or are all three NULL (then only
+ * rows and source info move).  With R*T == 0 only the layout + notify
+ * outputs are written.
+ */
+ep_status_t ep_layout_notify_dispatch(
+    const ep_shape_t* shape, const int64_t* topk_idx, const float* topk_w, const uint16_t* x,
+    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+    uint8_t* is_token_in_rank, int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+    int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+    int32_t* recv_channel_offset, int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+    int32_t* num_recv_tokens_per_expert, int64_t* recv_base, int32_t* send_pos, void* workspace,
+    size_t workspace_bytes, int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx, float* recv_topk_w,
+    int32_t* recv_src_info, int32_t* status, uint64_t* sched, int32_t* host_num_recv_tokens,
+    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Step 4 - combine.  [RT] intranodeCombine / internodeCombine (combined_x is
  * bf16, combined_topk_weights fp32), [AR] 4.2 (each received row returns to
  * its (src_rank, src_idx)).  For every source token (s,t):
@@ -518,6 +551,27 @@ ep_status_t ep_debug_layout_notify_tiled(
     int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens, int32_t* num_recv_tokens_per_expert,
     int64_t* recv_base, int32_t* send_pos, void* workspace, size_t workspace_bytes, int32_t* status,
     int32_t* host_num_recv_tokens, int32_t tile_tokens, int32_t stall_tile, int32_t wait_limit_us,
+    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Testing hook for failure detection in ep_layout_notify_dispatch.  Same
+ * arguments (no host_num_recv_tokens), with the layout + notify tile of
+ * ticket `stall_tile` (>= 0) withholding its lookback words and every wait
+ * bounded by `wait_limit_us` microseconds (1 .. 2e6).  The tiles that wait
+ * on it give up and go on (EP_DEV_TIMEOUT); the row map is then wrong but
+ * dispatch still writes no row outside the receive arrays; the context stays
+ * usable and a later call is exact.  Output contents are undefined after
+ * such a run.
+ */
+ep_status_t ep_debug_layout_notify_dispatch_stall(
+    const ep_shape_t* shape, const int64_t* topk_idx, const float* topk_w, const uint16_t* x,
+    int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+    uint8_t* is_token_in_rank, int32_t* rank_prefix_matrix, int32_t* gbl_channel_prefix_matrix,
+    int32_t* rdma_channel_prefix_matrix, int32_t* recv_gbl_rank_prefix_sum, int32_t* recv_rdma_rank_prefix_sum,
+    int32_t* recv_channel_offset, int32_t* num_recv_tokens, int32_t* num_rdma_recv_tokens,
+    int32_t* num_recv_tokens_per_expert, int64_t* recv_base, int32_t* send_pos, void* workspace,
+    size_t workspace_bytes, int64_t capacity_rows, uint16_t* recv_x, int64_t* recv_topk_idx, float* recv_topk_w,
+    int32_t* recv_src_info, int32_t* status, uint64_t* sched, int32_t stall_tile, int32_t wait_limit_us,
     cudaStream_t stream);
 
 #ifdef __cplusplus
