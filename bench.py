@@ -406,6 +406,92 @@ class Step:
         assert rc == 0, rc
 
 
+def per_config_leg(name: str, args, dev, peak: float) -> dict:
+    """One more workload, measured as the headline step is (CUDA-graph step with
+    the L2 flushed before every step, then each call alone between events),
+    with its own clock samples; no oracle and no end-to-end leg.  Its buffers
+    are freed before returning."""
+    from combine_get_dispatch_notify_gb300 import ep
+
+    w = CONFIGS[name]
+    sh = ep.EpShape.make(w.R, w.T, w.K, w.E, w.H, w.C, w.expert_alignment)
+    idx_h, wt_h = gen_routing(w)
+    x_d = gen_x(w, dev)
+    idx_d, wt_d = idx_h.to(dev), wt_h.to(dev)
+    pipe = ep.Pipeline(sh, worst_case_rows(w), str(dev))
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        step = Step(ep, pipe, x_d, idx_d, wt_d, stream)
+        step.all()
+        assert ep.ep_sync_status(pipe.status, stream) == ep.EP_OK, f"{name}: device status not OK"
+        P = int(pipe.notify["recv_base"][-1].item())
+        nbytes = algorithmic_bytes(w, P)
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step.all()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step.all()
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            g.replay()
+        torch.cuda.synchronize(dev)
+        ev_step, ev_ops = [], []
+        sampler = ClockSampler(dev.index)
+        with sampler:
+            pad_end = time.time() + 0.4
+            while time.time() < pad_end:
+                flush.fill_(1)
+                g.replay()
+            torch.cuda.synchronize(dev)
+            t0 = time.time()
+            for _ in range(args.steps):
+                flush.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                ev_step.append((a, b))
+            for _ in range(args.steps):
+                flush.fill_(1)
+                host_headroom()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                e[0].record(stream)
+                step.layout_notify()
+                e[1].record(stream)
+                step.dispatch()
+                e[2].record(stream)
+                step.combine()
+                e[3].record(stream)
+                ev_ops.append(e)
+            torch.cuda.synchronize(dev)
+            t1 = time.time()
+        assert ep.ep_sync_status(pipe.status, stream) == ep.EP_OK, f"{name}: device status not OK after timing"
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_step)
+    per_op = {}
+    for k, (j0, j1) in (("layout_notify", (0, 1)), ("dispatch", (1, 2)), ("combine", (2, 3))):
+        m = statistics.mean(e[j0].elapsed_time(e[j1]) for e in ev_ops)
+        gbs = nbytes[k] / (m * 1e-3) / 1e9
+        per_op[k] = {"us": round(m * 1e3, 2), "GB_per_s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+                     "algorithmic_bytes": nbytes[k]}
+        tr = recorded_traffic(k, w.name)
+        if tr is not None:
+            per_op[k]["dram_bytes"] = tr
+            per_op[k]["dram_frac_of_hbm"] = round(tr / (m * 1e-3) / 1e9 / peak, 4)
+    sb = step_bytes_of(nbytes)
+    out = {"workload": describe(w), "step_us": round(step_ms * 1e3, 2),
+           "value": round(sb / (step_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "tokens_per_s": round(w.R * w.T / (step_ms * 1e-3), 1), "rows_dispatched": P,
+           "layout_notify_form": "cluster" if step.ln_form == 1 else "tiled",
+           "per_op": per_op, "clocks": sampler.summary(t0 - 0.45, t1 + 0.05)}
+    del step, g, pipe, x_d, idx_d, wt_d, flush
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w):
     rank, local, world, dist = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -539,6 +625,40 @@ def run_ours(args, w):
     tok = w.R * w.T
     cached_bytes = tok * 2 * w.H + P * 2 * w.H + P * (2 * w.H + 4) + tok * 2 * w.H
     cached_total = sum_over_ranks(dist, cached_bytes)  # every rank joins the collective
+
+    # Layout, notify and dispatch as one launch (ep_layout_notify_dispatch)
+    # followed by combine, as a CUDA graph, beside the chain the headline times
+    fused = None
+    with torch.cuda.stream(stream):
+        D, Nt, La, Cb = pipe.dispatch, pipe.notify, pipe.layout, pipe.combine
+
+        def fused_step():
+            ep.ep_layout_notify_dispatch(sh, x_d, idx_d, wt_d, La, Nt, pipe.ln_workspace, D, pipe.status,
+                                         pipe.sched, stream=stream)
+            ep.ep_combine(sh, D["recv_x"], D["recv_topk_w"], Nt["send_pos"], Nt["recv_base"], Cb["combined_x"],
+                          Cb["combined_w"], pipe.status, stream)
+
+        fused_step()
+        gf = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf, stream=stream):
+            fused_step()
+        f_ms = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            gf.replay()
+            b.record(stream)
+            if i >= args.warmup:
+                f_ms.append((a, b))
+        torch.cuda.synchronize(dev)
+        assert ep.ep_sync_status(pipe.status, stream) == ep.EP_OK
+        fm = statistics.mean(a.elapsed_time(b) for a, b in f_ms)
+        fused = {"ms_per_step": round(fm, 5), "GB_per_s": round(step_bytes / (fm * 1e-3) / 1e9, 1),
+                 "vs_chain_step": round(fm / ms_local, 4),
+                 "note": "ep_layout_notify_dispatch (one launch) + ep_combine, CUDA graph, L2 flushed; "
+                         "the headline step is the chain ep_layout_notify -> ep_dispatch -> ep_combine"}
+        del gf
 
     # FP8 rows (the pages' 1-byte element size with per-token scales): dispatch alone
     fp8 = None
@@ -748,6 +868,13 @@ def run_ours(args, w):
                "ms_per_step": round(sec * 1e3, 2), "per_op_ms": dict(LAST_ORACLE_OPS_MS),
                "host": host_cpu()}
 
+    per_config = None
+    legs = [c for c in args.per_config.split(",") if c and c != "none" and c != w.name]
+    if world == 1 and legs:
+        # the headline holds under 10 GB; each leg frees its own buffers (the
+        # large workload needs ~76 GB)
+        per_config = {c: per_config_leg(c, args, dev, peak) for c in legs}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -762,6 +889,8 @@ def run_ours(args, w):
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": recorded_traffic(dom, w.name),
+                         "traffic_frac": (round(recorded_traffic(dom, w.name) / (dom_ms * 1e-3) / 1e9 / peak, 4)
+                                          if recorded_traffic(dom, w.name) is not None else None),
                          "algorithmic_bytes_per_launch": nbytes[dom]},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max, 4),
@@ -776,6 +905,8 @@ def run_ours(args, w):
                       ("as one cluster kernel" if step.ln_form == 1 else "as one tiled kernel") +
                       ", ep_dispatch, ep_combine); kernels chained by programmatic dependent launch",
             "ms_per_step_eager_with_op_events": round(eager_ms, 5),
+            "fused_layout_notify_dispatch": fused,
+            "per_config": per_config,
             "fp8_dispatch": fp8,
             "low_latency_layout": ll,
             "cached_mode": {"ms_per_step": round(cached_ms, 5),
@@ -798,10 +929,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work to time")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="tokens per rank instead of the workload's own (reduced-size profiling captures)")
+    ap.add_argument("--per-config", default="prefill,skewed,large",
+                    help="comma-separated further workloads measured into per_config (N=1 only), or none")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = CONFIGS[args.config]
+    if args.tokens is not None:
+        # same routing recipe, fewer tokens per rank (reduced-size profiling captures)
+        w = w.replace(T=args.tokens, name=f"{w.name}_T{args.tokens}")
     if args.impl == "reference":
         run_reference(args, w)
     else:
