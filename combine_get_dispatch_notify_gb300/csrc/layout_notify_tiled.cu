@@ -1,16 +1,19 @@
 // Steps 1 and 2 in one launch for shapes of any size: the tiled form (see
-// ln_tiled.cuh).  Persistent CTAs of 256 threads take tiles of TT tokens in
-// (source rank, tile) order from a ticket; the grid is what the device holds
-// at once, at most one CTA per tile.
+// ln_tiled.cuh).  Persistent CTAs take tiles of TT tokens in (source rank,
+// tile) order from a ticket; the grid is what the device holds at once, at
+// most one CTA per tile.  The tile size grows from 512 tokens until the tiles
+// fit one wave of 512-thread CTAs; CTAs have 512 threads then (256 when a
+// caller-chosen tile size leaves more tiles than that).
 #include "ln_tiled.cuh"
 
 namespace ep {
 namespace {
 
 constexpr int kTiledThreads = 256;
+constexpr int kTiledThreadsWide = 512;  // when the tiles fit one wave of 512-thread CTAs
 constexpr long long kMaxTiles = 16384;  // the tile size grows beyond this many tiles
 
-__global__ void __launch_bounds__(kTiledThreads) layout_notify_tiled_kernel(TiledLnArgs p) {
+__global__ void __launch_bounds__(kTiledThreadsWide) layout_notify_tiled_kernel(TiledLnArgs p) {
     extern __shared__ __align__(16) int32_t dyn[];
     __shared__ TiledShared sh;
     griddep_launch_dependents();
@@ -56,10 +59,11 @@ cudaError_t launch_layout_notify_tiled(const Shape& sh, const int64_t* topk_idx,
     const int sms = device_sm_count();
     int TT = tiled_tile_tokens(sh, tile_tokens);
     if (tile_tokens == 0) {
-        // larger tiles while the tiles are more than one wave of resident CTAs
+        // larger tiles while the tiles are more than one wave of resident
+        // 512-thread CTAs
         while (TT < 8192) {
             const long long tiles = static_cast<long long>(sh.R) * ((sh.T + TT - 1) / TT);
-            const int per = max_blocks_per_sm(kernel, kTiledThreads, tiled_smem_bytes(sh, TT));
+            const int per = max_blocks_per_sm(kernel, kTiledThreadsWide, tiled_smem_bytes(sh, TT));
             if (tiles <= static_cast<long long>(per) * sms) break;
             TT *= 2;
         }
@@ -69,12 +73,16 @@ cudaError_t launch_layout_notify_tiled(const Shape& sh, const int64_t* topk_idx,
     p.stall_tile = stall_tile;
     p.wait_limit_ns = wait_limit_ns;
     const size_t smem = tiled_smem_bytes(sh, TT);
-    const int per_sm = max_blocks_per_sm(kernel, kTiledThreads, smem);
+    // 512 threads per CTA (half the ids per thread) when every tile still
+    // gets a CTA of its own at once, else 256 (more CTAs resident)
+    const int per_wide = max_blocks_per_sm(kernel, kTiledThreadsWide, smem);
+    const int threads = p.n_tiles <= static_cast<long long>(per_wide) * sms ? kTiledThreadsWide : kTiledThreads;
+    const int per_sm = threads == kTiledThreadsWide ? per_wide : max_blocks_per_sm(kernel, kTiledThreads, smem);
     if (per_sm <= 0 || sms <= 0) return cudaErrorInvalidConfiguration;
     const long long cap = static_cast<long long>(per_sm) * sms;
     const long long grid = p.n_tiles < cap ? p.n_tiles : cap;
-    return launch_pdl(layout_notify_tiled_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTiledThreads), smem,
-                      stream, 0, false, p);
+    return launch_pdl(layout_notify_tiled_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, 0,
+                      false, p);
 }
 
 }  // namespace ep
