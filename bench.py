@@ -45,11 +45,13 @@ from combine_get_dispatch_notify_gb300.workloads import (CONFIGS, describe, gen_
 
 METRIC = "dispatch/combine HBM GB/s, µs & tokens/s (H=7168, top-8, 256 experts), 1×GB300"
 L2_FLUSH_BYTES = 256 << 20
+_CSRC = "combine_get_dispatch_notify_gb300/csrc/"
 KERNEL_SOURCES = {
-    "layout": "combine_get_dispatch_notify_gb300/csrc/layout.cu",
-    "notify": "combine_get_dispatch_notify_gb300/csrc/notify.cu",
-    "dispatch": "combine_get_dispatch_notify_gb300/csrc/dispatch.cu",
-    "combine": "combine_get_dispatch_notify_gb300/csrc/combine.cu",
+    "layout": (_CSRC + "layout.cu",),
+    "notify": (_CSRC + "notify.cu",),
+    "layout_notify": (_CSRC + "layout_notify.cu", _CSRC + "layout_notify_tiled.cu", _CSRC + "ln_tiled.cuh"),
+    "dispatch": (_CSRC + "dispatch.cu",),
+    "combine": (_CSRC + "combine.cu",),
 }
 
 
@@ -116,11 +118,16 @@ def code_text(src: str) -> str:
     return "\n".join(lines)
 
 
-def source_digest(rel: str) -> str:
-    """First 16 hex digits of the SHA-256 of a kernel source's code (comments and
-    blank lines left out)."""
-    with open(os.path.join(ROOT, rel)) as f:
-        return hashlib.sha256(code_text(f.read()).encode()).hexdigest()[:16]
+def source_digest(rels) -> str:
+    """First 16 hex digits of the SHA-256 of a kernel's source code (comments and
+    blank lines left out; several files are joined in order)."""
+    if isinstance(rels, str):
+        rels = (rels,)
+    text = []
+    for rel in rels:
+        with open(os.path.join(ROOT, rel)) as f:
+            text.append(code_text(f.read()))
+    return hashlib.sha256("\n".join(text).encode()).hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
