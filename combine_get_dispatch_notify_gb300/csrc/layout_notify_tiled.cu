@@ -2,8 +2,9 @@
 // ln_tiled.cuh).  Persistent CTAs take tiles of TT tokens in (source rank,
 // tile) order from a ticket; the grid is what the device holds at once, at
 // most one CTA per tile.  The tile size grows from 512 tokens until the tiles
-// fit one wave of 512-thread CTAs; CTAs have 512 threads then (256 when a
-// caller-chosen tile size leaves more tiles than that).
+// fit one wave of 512-thread CTAs, then shrinks to the smallest multiple of 32
+// that still does; CTAs have 512 threads then (256 when a caller-chosen tile
+// size leaves more tiles than that).
 #include "ln_tiled.cuh"
 
 namespace ep {
@@ -18,6 +19,7 @@ __global__ void __launch_bounds__(kTiledThreadsWide) layout_notify_tiled_kernel(
     __shared__ TiledShared sh;
     griddep_launch_dependents();
     griddep_wait();  // top-k ids written by the preceding kernel are visible
+    if (threadIdx.x == 0) tiled_prefetch_ids(p, static_cast<int>(blockIdx.x));
     const unsigned total_tickets = static_cast<unsigned>(p.n_tiles) + gridDim.x;
     for (;;) {
         const int b = tiled_take_ticket(p, sh, total_tickets);
@@ -66,6 +68,17 @@ cudaError_t launch_layout_notify_tiled(const Shape& sh, const int64_t* topk_idx,
             const int per = max_blocks_per_sm(kernel, kTiledThreadsWide, tiled_smem_bytes(sh, TT));
             if (tiles <= static_cast<long long>(per) * sms) break;
             TT *= 2;
+        }
+        // then the smallest tile (a multiple of 32) that still fits that wave:
+        // spreading the tokens over every resident slot shortens the busiest SM
+        if (TT > 512) {
+            const long long slots =
+                static_cast<long long>(max_blocks_per_sm(kernel, kTiledThreadsWide, tiled_smem_bytes(sh, TT))) * sms;
+            const long long per_source = slots / sh.R;
+            if (per_source >= 1) {
+                const long long tt = ((sh.T + per_source - 1) / per_source + kWarp - 1) / kWarp * kWarp;
+                if (tt < TT && tt * 2 > TT) TT = static_cast<int>(tt);
+            }
         }
     }
     TiledLnArgs p = tiled_args(sh, TT, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,

@@ -209,6 +209,17 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
     return x;
 }
 
+// Hint: bring the top-k ids of tile b into L2 (a CTA's first ticket is
+// usually its block index, so this overlaps the ticket's round trip).
+__device__ __forceinline__ void tiled_prefetch_ids(const TiledLnArgs& p, int b) {
+    if (b >= p.n_tiles) return;
+    const int s = b / p.tps, j = b - s * p.tps;
+    const int t0 = j * p.TT, t1 = min(t0 + p.TT, p.T);
+    if (t1 > t0)
+        prefetch_l2(p.topk_idx + (static_cast<int64_t>(s) * p.T + t0) * p.K,
+                    static_cast<size_t>(t1 - t0) * p.K * sizeof(int64_t));
+}
+
 // One tile b (of source b / tps).  `dyn` holds tiled_smem_words() words.
 // Every thread of the CTA calls it; blockDim.x is a multiple of 32.
 __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t* dyn, int b, unsigned seq) {
@@ -233,6 +244,7 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
     if (tid < V) {
         sh.fin[tid] = 0;
         sh.xs[tid] = 0;
+        sh.cnt[tid] = 0;
     }
     __syncthreads();
 
@@ -293,17 +305,31 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
         const uint32_t nb = node_bits(mask, R, N);
         const uint32_t word = nodes_in_word ? (mask | (nb << R)) : mask;
         const uint32_t tr = warp_transpose32(word, lane);
-        if (lane < V) bal[jj * Vp + lane] = tr;
+        if (lane < V) {
+            bal[jj * Vp + lane] = tr;
+            if (tr) atomicAdd(&sh.cnt[lane], __popc(tr));  // the tile's count per value
+        }
         if (!nodes_in_word) {
             for (int n = 0; n < N; ++n) {
                 const unsigned bb = __ballot_sync(0xffffffffu, (nb >> n) & 1u);
-                if (lane == 0) bal[jj * Vp + R + n] = bb;
+                if (lane == 0) {
+                    bal[jj * Vp + R + n] = bb;
+                    if (bb) atomicAdd(&sh.cnt[R + n], __popc(bb));
+                }
             }
         }
     }
     __syncthreads();
 
-    // B. warp per value: exclusive prefix of each 32-token block, tile count
+    // C1. publish the tile's counts at once (the first tile of a source: its
+    //     inclusive prefix), before the block prefixes below, so the tiles
+    //     after it can look back sooner
+    const bool withhold = b == p.stall_tile;
+    unsigned long long* mine = p.words + static_cast<int64_t>(b) * V;
+    if (tid < V && !withhold)
+        st_release_u64(mine + tid, lb_pack(seq, j == 0 ? kLbPrefix : kLbAggregate, static_cast<uint32_t>(sh.cnt[tid])));
+
+    // B. warp per value: exclusive prefix of each 32-token block
     {
         const int per = (Jt + kWarp - 1) / kWarp;
         for (int v = warp; v < V; v += warps) {
@@ -321,20 +347,13 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
                 pre[jj * Vp + v] = run;
                 run += __popc(bal[jj * Vp + v]);
             }
-            if (lane == kWarp - 1) sh.cnt[v] = inc;
         }
     }
-    __syncthreads();
 
-    // C. two-level scan.  (1) publish the counts (the first tile of a source:
-    //    its inclusive prefix) and look back over the source's earlier tiles;
-    //    (2) the source's last tile publishes the source total; (3) every tile
-    //    sums the totals of the earlier sources.
-    const bool withhold = b == p.stall_tile;
-    unsigned long long* mine = p.words + static_cast<int64_t>(b) * V;
-    if (tid < V && !withhold)
-        st_release_u64(mine + tid, lb_pack(seq, j == 0 ? kLbPrefix : kLbAggregate, static_cast<uint32_t>(sh.cnt[tid])));
-    // the tile's expert counts into the source's and the call's (red.add),
+    // C. two-level scan: (1, above) the counts are published; look back over
+    //    the source's earlier tiles; (2) the source's last tile publishes the
+    //    source total; (3) every tile sums the totals of the earlier sources.
+    // The tile's expert counts into the source's and the call's (red.add),
     // then, while the other warps look back, one thread of the last warp
     // arrives on their counters (after the barrier its fence orders every
     // thread's adds before the arrival), so the last tile of the source / of
