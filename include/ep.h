@@ -208,8 +208,8 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
  * 1-3).  Every output of both calls is written, with the same values.  Always
  * one kernel, in one of two forms (ep_layout_notify_fused tells which):
  *
- *   cluster form (R <= 16, R*T <= 4096, and a thread-block cluster of R CTAs
- *   fits on the device): CTA s counts source rank s's tokens and keeps one
+ *   cluster form (R <= 16, T <= 2048, R*T <= 16384, and a thread-block
+ *   cluster of R CTAs fits on the device): CTA s counts source rank s's tokens and keeps one
  *   ballot word per 32 tokens and destination in shared memory; the counts
  *   are exchanged through distributed shared memory and one cluster barrier,
  *   so no workspace traffic and no second pass over is_token_in_rank.
