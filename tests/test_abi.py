@@ -177,3 +177,24 @@ def test_c_consumer_compiles_links_and_runs(ep, tmp_path):
     assert int(ok) == ep.EP_OK and int(bad) == ep.EP_ERR_INVALID_ARG and int(nodes) == 2
     assert int(ws) == 256 + 16 * 8 * (16 + 2) * 8
     assert msg.strip() == "receive capacity exceeded"
+
+
+def test_layout_notify_workspace_bytes_follow_the_documented_formula(ep):
+    """Host-only: 256-byte header + 1 MiB + 32 KiB of expert counters + 8 (R+N)
+    bytes per tile + 8 R (R+N), with tiles of 512 tokens (fewer when T is
+    smaller, larger beyond 16384 tiles); 0 for an invalid shape."""
+    def want(R, T):
+        N = 1 if R <= 8 else R // 8
+        V = R + N
+        tt = 512 if T >= 512 else max(32, -(-T // 32) * 32)
+        while tt < 8192 and R * -(-T // tt) > 16384:
+            tt *= 2
+        tiles = R * (-(-T // tt) if T > 0 else 1)
+        return 256 + (1 << 20) + (32 << 10) + 8 * V * tiles + 8 * R * V
+
+    for R, T in [(1, 0), (2, 1), (3, 41), (8, 4096), (16, 8192), (32, 16384), (32, 20000), (16, 300),
+                 (32, 2 ** 25 - 1)]:  # R*T just under 2^30
+        sh = ep.EpShape.make(R, T, 8, R * 8, 7168, 24)  # E % R == 0
+        assert ep.ep_layout_notify_workspace_bytes(sh) == want(R, T), (R, T)
+    bad = ep.EpShape.make(12, 16, 8, 256, 7168, 24)  # R > 8 and not whole nodes
+    assert ep.ep_layout_notify_workspace_bytes(bad) == 0

@@ -232,3 +232,44 @@ def test_fused_first_call_inside_graph_capture_and_shared_workspace():
         assert ep.ep_sync_status(status) == ep.EP_OK
         check_layout_notify(lay2, nt2, lay_ref, nt_ref)
     assert int(sc.item()) == 0
+
+
+def test_fused_capacity_overflow_reports_status():
+    """A receive pool of half the rows: EP_ERR_CAPACITY, the rows that fit are
+    exact, and the rows just past the pool are left untouched."""
+    w = CASES["ragged_r16_zipf"]
+    idx, wt = gen_routing(w)
+    x = gen_x(w)
+    lay_ref, nt_ref, dp = _oracle_all(w, idx, wt, x)
+    cap = int(nt_ref["recv_base"][-1]) // 2
+    sh, lay, nt, full = _buffers(w, cap=cap + 8)
+    full["recv_x"].view(torch.int16).fill_(0x3C3C)
+    disp = {k: v[:cap] for k, v in full.items()}
+    ws = ep.alloc_layout_notify_workspace(sh)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_layout_notify_dispatch(sh, x.cuda(), idx.cuda(), wt.cuda(), lay, nt, ws, disp, status)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_CAPACITY
+    check_layout_notify(lay, nt, lay_ref, nt_ref)
+    _check_dispatch(disp, {k: v[:cap] for k, v in dp.items()}, cap)
+    assert bool((full["recv_x"][cap:].view(torch.int16) == 0x3C3C).all()), "rows past the pool were written"
+
+
+def test_fused_bad_expert_id_reports_status():
+    """Ids outside [-1, E): EP_ERR_INPUT; layout, notify and every dispatched
+    row and field are those of the top-k with those slots empty."""
+    w = CASES["r24_many_tiles"]
+    idx, wt = gen_routing(w)
+    x = gen_x(w)
+    idx[7, 0, 2] = w.E
+    idx[23, 1499, 5] = -9
+    clean = idx.clone()
+    clean[7, 0, 2] = -1
+    clean[23, 1499, 5] = -1
+    lay_ref, nt_ref, dp = _oracle_all(w, clean, wt, x)
+    sh, lay, nt, disp = _buffers(w)
+    ws = ep.alloc_layout_notify_workspace(sh)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_layout_notify_dispatch(sh, x.cuda(), idx.cuda(), wt.cuda(), lay, nt, ws, disp, status)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_INPUT
+    check_layout_notify(lay, nt, lay_ref, nt_ref)
+    _check_dispatch(disp, dp, int(nt_ref["recv_base"][-1]))

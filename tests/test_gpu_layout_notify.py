@@ -342,3 +342,32 @@ def test_tiled_refuses_bad_tile_sizes_and_small_workspace():
     with pytest.raises(ValueError):
         ep.ep_layout_notify(sh, idx.cuda(), lay, nt, small, status)
     assert ep.ep_sync_status(status) == ep.EP_OK  # nothing was enqueued
+
+
+def test_tiled_bad_expert_id_reports_status():
+    """Ids outside [-1, E) in the tiled form: EP_ERR_INPUT, and every output is
+    that of the top-k with those slots empty."""
+    w = Workload("e", R=24, T=300, H=64, E=96, K=6, C=7, mask=0.1)
+    idx, _ = gen_routing(w)
+    idx[3, 5, 1] = w.E + 7
+    idx[20, 299, 5] = -5
+    sh, lay, nt, status, ws = _tiled(w, idx, 64)
+    assert ep.ep_sync_status(status) == ep.EP_ERR_INPUT
+    clean = idx.clone()
+    clean[3, 5, 1] = -1
+    clean[20, 299, 5] = -1
+    lay_ref, nt_ref = _oracle(w, clean)
+    check_layout_notify(lay, nt, lay_ref, nt_ref)
+    assert int((ws[256:256 + (1 << 20) + (32 << 10)] != 0).sum()) == 0
+
+
+def test_tiled_every_expert_counter_in_use():
+    """32 ranks and 8192 experts: the tiled form's expert counters are used in
+    full ([32][8192]); results exact, counters left zero."""
+    w = Workload("e", R=32, T=64, H=64, E=8192, K=16, C=3, routing="replace", mask=0.05)
+    idx, _ = gen_routing(w)
+    lay_ref, nt_ref = _oracle(w, idx)
+    sh, lay, nt, status, ws = _tiled(w, idx, 32)
+    assert ep.ep_sync_status(status) == ep.EP_OK
+    check_layout_notify(lay, nt, lay_ref, nt_ref)
+    assert int((ws[256:256 + (1 << 20) + (32 << 10)] != 0).sum()) == 0
