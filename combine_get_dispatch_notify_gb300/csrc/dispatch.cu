@@ -444,11 +444,13 @@ layout_notify_dispatch_kernel(DispatchArgs p, TiledLnArgs ln, uint32_t tile_smem
     const Ring rg = ring_setup(p, smem);
     ring_prologue(p, rg);
     griddep_wait();  // top-k ids written by the preceding kernel are visible
-    if (threadIdx.x == 0) tiled_prefetch_ids(ln, static_cast<int>(blockIdx.x));
+    // Thread 0 is held while its row copies are taken in, thread 32 while the
+    // ids prefetch is: a third thread takes the tickets.
+    if (threadIdx.x == kWarp) tiled_prefetch_ids(ln, static_cast<int>(blockIdx.x));
     int32_t* dyn = reinterpret_cast<int32_t*>(smem + tile_smem_off);
     const unsigned total_tickets = static_cast<unsigned>(ln.n_tiles) + gridDim.x;
     for (;;) {
-        const int b = tiled_take_ticket(ln, sh, total_tickets);
+        const int b = tiled_take_ticket(ln, sh, total_tickets, 2 * kWarp);
         if (b < 0) break;
         tiled_tile(ln, sh, dyn, b, sh.seq);
     }

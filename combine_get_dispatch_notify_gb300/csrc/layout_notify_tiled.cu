@@ -19,7 +19,9 @@ __global__ void __launch_bounds__(kTiledThreadsWide) layout_notify_tiled_kernel(
     __shared__ TiledShared sh;
     griddep_launch_dependents();
     griddep_wait();  // top-k ids written by the preceding kernel are visible
-    if (threadIdx.x == 0) tiled_prefetch_ids(p, static_cast<int>(blockIdx.x));
+    // The issuing thread is held while the prefetch is taken in: not the one
+    // that takes the ticket.
+    if (threadIdx.x == kWarp) tiled_prefetch_ids(p, static_cast<int>(blockIdx.x));
     const unsigned total_tickets = static_cast<unsigned>(p.n_tiles) + gridDim.x;
     for (;;) {
         const int b = tiled_take_ticket(p, sh, total_tickets);

@@ -156,11 +156,12 @@ struct TiledShared {
     int last_of_source, last_of_all;
 };
 
-// Takes the next ticket of the call (thread 0) and shares it with the CTA.
-// Returns the tile index, or -1 once every tile is taken.  The ticket that
-// completes the call's count arms the next call.
-__device__ __forceinline__ int tiled_take_ticket(const TiledLnArgs& p, TiledShared& sh, unsigned total_tickets) {
-    if (threadIdx.x == 0) {
+// Takes the next ticket of the call (thread `taker`) and shares it with the
+// CTA.  Returns the tile index, or -1 once every tile is taken.  The ticket
+// that completes the call's count arms the next call.
+__device__ __forceinline__ int tiled_take_ticket(const TiledLnArgs& p, TiledShared& sh, unsigned total_tickets,
+                                                 int taker = 0) {
+    if (static_cast<int>(threadIdx.x) == taker) {
         const unsigned long long old = atomicAdd(p.ticket, 1ull);
         const unsigned taken = static_cast<unsigned>(old & 0xffffffffull);
         const unsigned seq = static_cast<unsigned>(old >> 32) + 1u;
