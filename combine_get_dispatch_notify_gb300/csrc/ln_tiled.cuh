@@ -12,15 +12,17 @@
 //   B. warp per value (rank or node): the tile's count and the exclusive
 //      prefix of every 32-token block inside the tile;
 //   C. two-level single-pass scan ([AR] 3.2: prefix sums by a block scan):
-//      a tile publishes its counts; adds its histogram into the source's and
-//      the call's expert counters (red.add); then looks back over the earlier
-//      tiles of its own source (decoupled lookback, 32 predecessors per
-//      probe, every value at once); the source's last tile publishes the
-//      source total;
-//      every tile adds the totals of the earlier source ranks.  Tiles are
-//      ordered by source rank first, so the result - the global exclusive
-//      prefix of rank r at the tile - is exactly the row, inside r's receive
-//      region, of the tile's first token routed to r;
+//      a tile publishes its counts, and adds them into its source's total
+//      words (one 64-bit atomic per value: the tiles that have added in the
+//      high half, the running total in the low half); adds its histogram into
+//      the source's and the call's expert counters (red.add); then looks back
+//      over the earlier tiles of its own source (decoupled lookback, 32
+//      predecessors per probe, every value at once) and adds the totals of
+//      the earlier source ranks, each read once all of that source's tiles
+//      have added into it.  Tiles are ordered by source rank first, so the
+//      result - the global exclusive prefix of rank r at the tile - is
+//      exactly the row, inside r's receive region, of the tile's first token
+//      routed to r;
 //   D. the tile's outputs: send_pos of its tokens; the channel boundaries
 //      inside it (recv_channel_offset at a channel's first token,
 //      gbl/rdma_channel_prefix_matrix at its end); for the source's last
@@ -32,11 +34,11 @@
 //      the next call), the last tile of the call does the same for the
 //      per-expert receive counts.
 // Only steps C and E wait, and only on tiles with smaller tickets (earlier
-// tiles of the source; the last tiles of earlier sources), which were taken
-// by CTAs that are already running and publish what is waited for before
-// waiting on anything outside their own source; so the scan needs no
-// co-residency and always finishes, in a few probes whatever the number of
-// tiles.  Every wait is bounded (EP_DEV_TIMEOUT).
+// tiles of the source; the tiles of earlier sources), which were taken by
+// CTAs that are already running and publish what is waited for before they
+// wait on anything; so the scan needs no co-residency and always finishes,
+// in a few probes whatever the number of tiles.  Every wait is bounded
+// (EP_DEV_TIMEOUT).
 #pragma once
 
 #include "ep_device.cuh"
@@ -48,6 +50,7 @@ constexpr int kTiledMaxValues = 64;  // R + N <= 32 + 4
 constexpr int kLbSlots = 32;         // predecessors read per lookback probe
 constexpr int kAccRanks = 32;
 constexpr int kAccExperts = 8192;
+constexpr int kBankWords = 32 * 36;  // source total words of one call: [R][V], R <= 32, V <= 36
 
 // Workspace of the tiled form, all offsets in bytes from its start:
 //   header     ticket word, arrival counters (all tiles, finished tiles, one
@@ -55,14 +58,17 @@ constexpr int kAccExperts = 8192;
 //   acc        expert counts of the running call, per source [32][8192] and
 //              summed over sources [8192], int32, whatever the shape (so a
 //              later call of another shape finds them zero);
-//   words      64-bit words tagged with the writing call's sequence number:
-//              within-source lookback words [n_tiles][V] and source totals
-//              [R][V], so what an earlier call of any shape left there never
-//              reads as this call's.
-// The header counters and acc must be zero before the first call; every
-// call leaves them zero.
+//   banks      two banks of source total words [32 * 36] (64-bit: tiles in
+//              [63:32], total in [31:0]); a call adds into the bank of its
+//              sequence number's parity, and its first tile clears the other
+//              one for the next call;
+//   words      within-source lookback words [n_tiles][V], tagged with the
+//              writing call's sequence number, so what an earlier call of any
+//              shape left there never reads as this call's.
+// The header counters, acc and banks must be zero before the first call;
+// every call leaves the counters and acc zero, and the next call's bank.
 struct TiledWorkspace {
-    size_t ticket, arrive_all, finished, ready, src_arrive, acc, acc_all, words, totals, total;
+    size_t ticket, arrive_all, finished, ready, src_arrive, acc, acc_all, banks, words, total;
 };
 
 inline TiledWorkspace tiled_workspace_layout(int R, int N, long long n_tiles) {
@@ -75,9 +81,9 @@ inline TiledWorkspace tiled_workspace_layout(int R, int N, long long n_tiles) {
     w.src_arrive = 64;  // R <= 32 counters
     w.acc = 256;
     w.acc_all = w.acc + sizeof(int32_t) * static_cast<size_t>(kAccRanks) * kAccExperts;
-    w.words = w.acc_all + sizeof(int32_t) * static_cast<size_t>(kAccExperts);
-    w.totals = w.words + sizeof(unsigned long long) * static_cast<size_t>(n_tiles) * V;
-    w.total = w.totals + sizeof(unsigned long long) * static_cast<size_t>(R) * V;
+    w.banks = w.acc_all + sizeof(int32_t) * static_cast<size_t>(kAccExperts);
+    w.words = w.banks + sizeof(unsigned long long) * 2 * static_cast<size_t>(kBankWords);
+    w.total = w.words + sizeof(unsigned long long) * static_cast<size_t>(n_tiles) * V;
     return w;
 }
 
@@ -95,8 +101,8 @@ struct TiledLnArgs {
     unsigned* src_arrive;        // [R] tiles of each source whose expert counts are in
     int32_t* acc;                // [32][8192] per-source expert counts of the running call
     int32_t* acc_all;            // [8192] expert counts summed over sources
+    unsigned long long* banks;   // [2][32 * 36] source total words, by call parity
     unsigned long long* words;   // [n_tiles][V] lookback words, within each source
-    unsigned long long* totals;  // [R][V] tagged per-source totals
     int R, T, K, E, N, E_loc, C, q, align, V, TT, tps, n_tiles;
     int Ep, Vp;           // E and V rounded up to 4 (shared-memory row strides)
     uint32_t eloc_magic;  // ceil(2^32 / E_loc): e / E_loc = umulhi(e, magic) for e < 8192, E_loc >= 2
@@ -133,6 +139,23 @@ __device__ __forceinline__ unsigned long long lb_wait(const unsigned long long* 
         word = ld_acquire_u64(w);
     }
     return word;
+}
+
+// Total of a source once all `tiles` of its tiles have added into its word
+// (waiting, bounded); on timeout 0 and `timed_out` set.
+__device__ __forceinline__ int32_t bank_wait(const unsigned long long* w, unsigned tiles, long long deadline,
+                                             bool& timed_out) {
+    unsigned long long word = ld_acquire_u64(w);
+    uint32_t polls = 0;
+    while (static_cast<unsigned>(word >> 32) != tiles) {
+        if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
+            timed_out = true;
+            return 0;
+        }
+        __nanosleep(32);
+        word = ld_acquire_u64(w);
+    }
+    return static_cast<int32_t>(word & 0xffffffffull);
 }
 
 // Dynamic shared memory of one tile, in 4-byte words: the expert histogram
@@ -240,6 +263,11 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
     const long long deadline = globaltimer_ns() + p.wait_limit_ns;
     bool timed_out = false;
 
+    unsigned long long* bank = p.banks + (seq & 1u) * kBankWords;  // this call's source totals
+    if (b == 0) {  // the previous call is complete: its bank is the next call's
+        unsigned long long* other = p.banks + ((seq + 1u) & 1u) * kBankWords;
+        for (int i = tid; i < kBankWords; i += B) other[i] = 0ull;
+    }
     for (int i = tid; i < E; i += B) hist[i] = 0;
     for (int i = tid; i < ntok; i += B) tmask[i] = 0u;
     if (tid < V) {
@@ -323,12 +351,15 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
     __syncthreads();
 
     // C1. publish the tile's counts at once (the first tile of a source: its
-    //     inclusive prefix), before the block prefixes below, so the tiles
-    //     after it can look back sooner
+    //     inclusive prefix) and add them into the source's totals, before the
+    //     block prefixes below, so the tiles after it can read them sooner
     const bool withhold = b == p.stall_tile;
     unsigned long long* mine = p.words + static_cast<int64_t>(b) * V;
-    if (tid < V && !withhold)
-        st_release_u64(mine + tid, lb_pack(seq, j == 0 ? kLbPrefix : kLbAggregate, static_cast<uint32_t>(sh.cnt[tid])));
+    if (tid < V && !withhold) {
+        const uint32_t c = static_cast<uint32_t>(sh.cnt[tid]);
+        st_release_u64(mine + tid, lb_pack(seq, j == 0 ? kLbPrefix : kLbAggregate, c));
+        atomicAdd(bank + s * V + tid, (1ull << 32) | c);
+    }
 
     // B. warp per value: exclusive prefix of each 32-token block
     {
@@ -351,9 +382,9 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
         }
     }
 
-    // C. two-level scan: (1, above) the counts are published; look back over
-    //    the source's earlier tiles; (2) the source's last tile publishes the
-    //    source total; (3) every tile sums the totals of the earlier sources.
+    // C. two-level scan: (1, above) the counts are published and added into
+    //    the source's totals; (2) look back over the source's earlier tiles;
+    //    (3) sum the totals of the earlier sources.
     // The tile's expert counts into the source's and the call's (red.add),
     // then, while the other warps look back, one thread of the last warp
     // arrives on their counters (after the barrier its fence orders every
@@ -410,7 +441,6 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
         if (!withhold) {
             const uint32_t incl = static_cast<uint32_t>(wex + sh.cnt[tid]);
             if (j > 0) st_release_u64(mine + tid, lb_pack(seq, kLbPrefix, incl));
-            if (last_tile) st_release_u64(p.totals + static_cast<int64_t>(s) * V + tid, lb_pack(seq, 0u, incl));
         }
     }
     {
@@ -420,7 +450,7 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
                 v -= V;
                 ++s2;
             }
-            atomicAdd(&sh.xs[v], lb_val(lb_wait(p.totals + static_cast<int64_t>(s2) * V + v, seq, deadline, timed_out)));
+            atomicAdd(&sh.xs[v], bank_wait(bank + s2 * V + v, static_cast<unsigned>(p.tps), deadline, timed_out));
         }
     }
     __syncthreads();
@@ -522,8 +552,8 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
             int32_t run = 0;
             for (int m = 0; m < N; ++m) {
                 const int peer = m * kNodeSize + r % kNodeSize;
-                run += lb_val(lb_wait(p.totals + static_cast<int64_t>(peer) * V + R + r / kNodeSize, seq, deadline,
-                                      timed_out));
+                run += bank_wait(bank + peer * V + R + r / kNodeSize, static_cast<unsigned>(p.tps), deadline,
+                                 timed_out);
                 p.a.recv_rdma_rank_prefix_sum[static_cast<int64_t>(r) * N + m] = run;
             }
             p.a.num_rdma_recv_tokens[r] = run;
@@ -607,8 +637,8 @@ inline TiledLnArgs tiled_args(const Shape& sh, int TT, const int64_t* topk_idx, 
     p.src_arrive = reinterpret_cast<unsigned*>(base + w.src_arrive);
     p.acc = reinterpret_cast<int32_t*>(base + w.acc);
     p.acc_all = reinterpret_cast<int32_t*>(base + w.acc_all);
+    p.banks = reinterpret_cast<unsigned long long*>(base + w.banks);
     p.words = reinterpret_cast<unsigned long long*>(base + w.words);
-    p.totals = reinterpret_cast<unsigned long long*>(base + w.totals);
     return p;
 }
 

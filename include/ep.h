@@ -250,7 +250,8 @@ ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
 
 /* Bytes of workspace ep_layout_notify (and ep_layout_notify_dispatch) needs
  * for `shape`, or 0 for an invalid shape: a 256-byte header, 1 MiB + 32 KiB
- * of per-expert counters, 8 * (R + N) bytes per tile and 8 * R * (R + N). */
+ * of per-expert counters, 18 KiB of per-source totals (two banks of 32 * 36
+ * 64-bit words) and 8 * (R + N) bytes per tile. */
 size_t ep_layout_notify_workspace_bytes(const ep_shape_t* shape);
 
 /* Which kernel ep_layout_notify runs for this shape on the current device:

@@ -238,7 +238,7 @@ def _tiled_ws_bytes(w: Workload, tile_tokens: int) -> int:
     if tile_tokens == 0:
         return ep.ep_layout_notify_workspace_bytes(sh)
     tiles = w.R * (max(1, -(-w.T // tile_tokens)) if w.T > 0 else 1)
-    return 256 + (1 << 20) + (32 << 10) + 8 * (w.R + w.N) * tiles + 8 * w.R * (w.R + w.N)
+    return 256 + (1 << 20) + (32 << 10) + (18 << 10) + 8 * (w.R + w.N) * tiles
 
 
 TILED_SIZES = (32, 96, 512, 0)
@@ -282,6 +282,10 @@ def test_tiled_workspace_serves_shapes_in_turn_and_stays_clean():
         assert (head[8:16] == 0).all()                               # tiles arrived / finished
         assert (head[64:192] == 0).all()                             # tiles arrived per source
         assert int((ws[256:256 + (1 << 20) + (32 << 10)] != 0).sum()) == 0  # expert counters
+        seq = int(head[:8].numpy().view(np.uint64)[0]) >> 32                # this call's sequence number
+        banks = 256 + (1 << 20) + (32 << 10)
+        nxt = banks + ((seq + 1) & 1) * (9 << 10)
+        assert int((ws[nxt:nxt + (9 << 10)] != 0).sum()) == 0               # the next call's source totals
 
 
 def test_tiled_stall_times_out_and_next_call_is_exact():
