@@ -429,12 +429,13 @@ __device__ void dispatch_roles(const DispatchArgs& p, const Ring& rg) {
 // Layout, notify and dispatch in one launch ([RT] internodeNotifyDispatch
 // followed by internodeDispatch; the pages' notify hands its results to
 // dispatch through per-channel head/tail words, here through one `ready`
-// word).  The dispatch CTAs load their first ring-full of x rows, then take
-// layout + notify tiles from the tiled form's ticket (see ln_tiled.cuh) until
-// none is left, then wait - bounded - until the call's row map is complete
-// and run the dispatch roles on it, reading send_pos and recv_base through
-// L2 since this launch wrote them.  A CTA waits only on tiles taken by CTAs
-// that are already running, so no co-residency is needed.
+// word).  The dispatch CTAs load their first ring-full of x rows, then work
+// on layout + notify tiles as the tiled form's kernel does (see ln_tiled.cuh:
+// the first tile by block index, later ones by ticket) until none is left,
+// then wait - bounded - until the call's row map is complete and run the
+// dispatch roles on it, reading send_pos and recv_base through L2 since this
+// launch wrote them.  A CTA waits only on tiles of CTAs that are already
+// running, so no co-residency is needed.
 __global__ void __launch_bounds__(kDispatchThreads)
 layout_notify_dispatch_kernel(DispatchArgs p, TiledLnArgs ln, uint32_t tile_smem_off) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -448,12 +449,12 @@ layout_notify_dispatch_kernel(DispatchArgs p, TiledLnArgs ln, uint32_t tile_smem
     // ids prefetch is: a third thread takes the tickets.
     if (threadIdx.x == kWarp) tiled_prefetch_ids(ln, static_cast<int>(blockIdx.x));
     int32_t* dyn = reinterpret_cast<int32_t*>(smem + tile_smem_off);
-    const unsigned total_tickets = static_cast<unsigned>(ln.n_tiles) + gridDim.x;
-    for (;;) {
-        const int b = tiled_take_ticket(ln, sh, total_tickets, 2 * kWarp);
-        if (b < 0) break;
-        tiled_tile(ln, sh, dyn, b, sh.seq);
+    int b = blockIdx.x < static_cast<unsigned>(ln.n_tiles) ? static_cast<int>(blockIdx.x) : -1;
+    if (b < 0) {  // no tile of its own: one ticket, for the call's sequence number
+        if (threadIdx.x == 2 * kWarp) tiled_ticket_done(ln, sh, atomicAdd(ln.ticket, 1ull));
+        __syncthreads();
     }
+    while (b >= 0) b = tiled_tile(ln, sh, dyn, b, 2 * kWarp);
     const unsigned long long seq = sh.seq;
     if (threadIdx.x == 0) {
         const long long deadline = globaltimer_ns() + p.wait_limit_ns;

@@ -1,7 +1,7 @@
 // Steps 1 and 2 in one launch for shapes of any size: the tiled form (see
 // ln_tiled.cuh).  Persistent CTAs take tiles of TT tokens in (source rank,
-// tile) order from a ticket; the grid is what the device holds at once, at
-// most one CTA per tile.  The tile size grows from 512 tokens until the tiles
+// tile) order, the first by block index and later ones from a ticket; the
+// grid is what the device holds at once, at most one CTA per tile.  The tile size grows from 512 tokens until the tiles
 // fit one wave of 512-thread CTAs, then shrinks to the smallest multiple of 32
 // that still does; CTAs have 512 threads then (256 when a caller-chosen tile
 // size leaves more tiles than that).
@@ -20,14 +20,10 @@ __global__ void __launch_bounds__(kTiledThreadsWide) layout_notify_tiled_kernel(
     griddep_launch_dependents();
     griddep_wait();  // top-k ids written by the preceding kernel are visible
     // The issuing thread is held while the prefetch is taken in: not the one
-    // that takes the ticket.
+    // that takes the tickets.
     if (threadIdx.x == kWarp) tiled_prefetch_ids(p, static_cast<int>(blockIdx.x));
-    const unsigned total_tickets = static_cast<unsigned>(p.n_tiles) + gridDim.x;
-    for (;;) {
-        const int b = tiled_take_ticket(p, sh, total_tickets);
-        if (b < 0) break;
-        tiled_tile(p, sh, dyn, b, sh.seq);
-    }
+    int b = static_cast<int>(blockIdx.x);  // the grid is at most one CTA per tile
+    while (b >= 0) b = tiled_tile(p, sh, dyn, b, 0);
 }
 
 }  // namespace

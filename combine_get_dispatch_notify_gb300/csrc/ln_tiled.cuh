@@ -3,8 +3,9 @@
 // The same results as the layout step ([RT] getDispatchLayout; the count
 // vectors of [IN] notify_dispatch sm0 stage 3) followed by notify ([IN]
 // sm1..x stages 1-3 and sm0 stage 6), computed by CTAs that each take tiles
-// of up to TT tokens of one source rank, in (source rank, tile) order by an
-// atomic ticket:
+// of up to TT tokens of one source rank, tiles numbered in (source rank,
+// tile) order: a CTA's first tile is its block index, its later ones come
+// from an atomic ticket counter:
 //   A. thread per (token, pair of top-k slots), up to 8 pairs of a thread
 //      loaded at once: expert histogram in shared memory and the token's rank
 //      mask; warp per 32 tokens writes the is_token_in_rank rows and one
@@ -27,17 +28,21 @@
 //      inside it (recv_channel_offset at a channel's first token,
 //      gbl/rdma_channel_prefix_matrix at its end); for the source's last
 //      tile the source's counts and rank prefix;
-//   E. the tile with the last ticket - it holds the global prefix at the
-//      very end - writes the receive counts, recv_base and the node-level
+//   E. the last tile - it holds the global prefix at the very end - writes
+//      the receive counts, recv_base and the node-level
 //      receive prefix; every tile arrives on two counters, and the last tile
 //      of a source copies the source's expert counts out (clearing them for
 //      the next call), the last tile of the call does the same for the
 //      per-expert receive counts.
-// Only steps C and E wait, and only on tiles with smaller tickets (earlier
-// tiles of the source; the tiles of earlier sources), which were taken by
-// CTAs that are already running and publish what is waited for before they
-// wait on anything; so the scan needs no co-residency and always finishes,
-// in a few probes whatever the number of tiles.  Every wait is bounded
+// Only steps C and E wait, and only on tiles with smaller numbers (earlier
+// tiles of the source; the tiles of earlier sources), which publish what is
+// waited for before they wait on anything.  A smaller number is either the
+// first tile of a CTA with a smaller block index - dispatched before this
+// CTA, as blocks are dispatched in index order (the order a single-pass scan
+// with decoupled look-back relies on), so already running or done - or a
+// ticket taken earlier by a running CTA, which works on it after its current
+// (smaller) tile.  So the scan needs no co-residency and finishes in a few
+// probes whatever the number of tiles; every wait is bounded
 // (EP_DEV_TIMEOUT).
 #pragma once
 
@@ -179,22 +184,22 @@ struct TiledShared {
     int last_of_source, last_of_all;
 };
 
-// Takes the next ticket of the call (thread `taker`) and shares it with the
-// CTA.  Returns the tile index, or -1 once every tile is taken.  The ticket
-// that completes the call's count arms the next call.
-__device__ __forceinline__ int tiled_take_ticket(const TiledLnArgs& p, TiledShared& sh, unsigned total_tickets,
-                                                 int taker = 0) {
-    if (static_cast<int>(threadIdx.x) == taker) {
-        const unsigned long long old = atomicAdd(p.ticket, 1ull);
-        const unsigned taken = static_cast<unsigned>(old & 0xffffffffull);
-        const unsigned seq = static_cast<unsigned>(old >> 32) + 1u;
-        if (taken == total_tickets - 1u) atomicExch(p.ticket, static_cast<unsigned long long>(seq) << 32);
-        if (taken >= total_tickets) flag_error(p.a.status, EP_DEV_INCONSISTENT);  // workspace not zeroed
-        sh.ticket = taken < static_cast<unsigned>(p.n_tiles) ? static_cast<int>(taken) : -1;
-        sh.seq = seq;
-    }
-    __syncthreads();
-    return sh.ticket;
+// Tickets: a CTA's first tile is its block index; every CTA takes one ticket
+// per tile it works on (a CTA without a first tile, one ticket), max(n_tiles,
+// grid) tickets in all, and ticket t names tile grid + t (none once that is
+// n_tiles or more).  A ticket also carries the call's sequence number (the
+// previous call's, in the high half, plus one).  Decodes a ticket taken by
+// this thread into sh.seq and sh.ticket (the CTA's next tile, or -1); the
+// ticket that completes the count arms the next call.
+__device__ __forceinline__ void tiled_ticket_done(const TiledLnArgs& p, TiledShared& sh, unsigned long long old) {
+    const unsigned taken = static_cast<unsigned>(old & 0xffffffffull);
+    const unsigned seq = static_cast<unsigned>(old >> 32) + 1u;
+    const unsigned total = max(static_cast<unsigned>(p.n_tiles), gridDim.x);
+    if (taken == total - 1u) atomicExch(p.ticket, static_cast<unsigned long long>(seq) << 32);
+    if (taken >= total) flag_error(p.a.status, EP_DEV_INCONSISTENT);  // workspace not zeroed
+    const long long next = static_cast<long long>(gridDim.x) + taken;
+    sh.ticket = next < p.n_tiles ? static_cast<int>(next) : -1;
+    sh.seq = seq;
 }
 
 // Prefix of value v before local token lt of the tile (0 <= lt <= ntok).
@@ -233,8 +238,8 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
     return x;
 }
 
-// Hint: bring the top-k ids of tile b into L2 (a CTA's first ticket is
-// usually its block index, so this overlaps the ticket's round trip).
+// Hint: bring the top-k ids of tile b into L2 (a CTA's first tile, whose
+// loads start straight away).
 __device__ __forceinline__ void tiled_prefetch_ids(const TiledLnArgs& p, int b) {
     if (b >= p.n_tiles) return;
     const int s = b / p.tps, j = b - s * p.tps;
@@ -244,9 +249,12 @@ __device__ __forceinline__ void tiled_prefetch_ids(const TiledLnArgs& p, int b) 
                     static_cast<size_t>(t1 - t0) * p.K * sizeof(int64_t));
 }
 
-// One tile b (of source b / tps).  `dyn` holds tiled_smem_words() words.
+// One tile b (of source b / tps); returns the CTA's next tile, or -1.  Thread
+// `taker` takes the next ticket as the tile starts and reads it (the call's
+// sequence number with it) only once the tile's counts are in, so its round
+// trip overlaps the tile's loads.  `dyn` holds tiled_smem_words() words.
 // Every thread of the CTA calls it; blockDim.x is a multiple of 32.
-__device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t* dyn, int b, unsigned seq) {
+__device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t* dyn, int b, int taker) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = static_cast<int>(blockDim.x), warps = B >> 5;
     const int R = p.R, N = p.N, V = p.V, K = p.K, T = p.T, E = p.E, C = p.C;
@@ -262,12 +270,9 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
     int32_t* pre = reinterpret_cast<int32_t*>(bal + J * Vp);
     const long long deadline = globaltimer_ns() + p.wait_limit_ns;
     bool timed_out = false;
+    unsigned long long ticket = 0;
+    if (tid == taker) ticket = atomicAdd(p.ticket, 1ull);
 
-    unsigned long long* bank = p.banks + (seq & 1u) * kBankWords;  // this call's source totals
-    if (b == 0) {  // the previous call is complete: its bank is the next call's
-        unsigned long long* other = p.banks + ((seq + 1u) & 1u) * kBankWords;
-        for (int i = tid; i < kBankWords; i += B) other[i] = 0ull;
-    }
     for (int i = tid; i < E; i += B) hist[i] = 0;
     for (int i = tid; i < ntok; i += B) tmask[i] = 0u;
     if (tid < V) {
@@ -348,7 +353,14 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
             }
         }
     }
+    if (tid == taker) tiled_ticket_done(p, sh, ticket);
     __syncthreads();
+    const unsigned seq = sh.seq;
+    unsigned long long* bank = p.banks + (seq & 1u) * kBankWords;  // this call's source totals
+    if (b == 0) {  // the previous call is complete: its bank is the next call's
+        unsigned long long* other = p.banks + ((seq + 1u) & 1u) * kBankWords;
+        for (int i = tid; i < kBankWords; i += B) other[i] = 0ull;
+    }
 
     // C1. publish the tile's counts at once (the first tile of a source: its
     //     inclusive prefix) and add them into the source's totals, before the
@@ -595,6 +607,7 @@ __device__ inline void tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t
         }
     }
     __syncthreads();  // shared state is reused by the CTA's next tile
+    return sh.ticket;
 }
 
 // Fills the argument block (host).  `workspace` is laid out by
