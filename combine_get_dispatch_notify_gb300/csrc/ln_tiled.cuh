@@ -117,7 +117,10 @@ struct TiledLnArgs {
 };
 
 // Tagged word: [63:32] sequence number of the writing call, [31:30] flag,
-// [29:0] value.  A word of another call reads as "not yet published".
+// [29:0] value.  A word of another call reads as "not yet published".  The
+// word is the whole message - nothing else is read on the strength of it -
+// so it is stored and polled with relaxed gpu-scope accesses, as are the
+// source total words.
 constexpr unsigned kLbAggregate = 1u;
 constexpr unsigned kLbPrefix = 2u;
 
@@ -133,7 +136,7 @@ __device__ __forceinline__ int32_t lb_val(unsigned long long w) {
 // On timeout returns a prefix word of value 0 and sets `timed_out`.
 __device__ __forceinline__ unsigned long long lb_wait(const unsigned long long* w, unsigned seq,
                                                       long long deadline, bool& timed_out) {
-    unsigned long long word = ld_acquire_u64(w);
+    unsigned long long word = ld_relaxed_u64(w);
     uint32_t polls = 0;
     while (static_cast<unsigned>(word >> 32) != seq) {
         if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
@@ -141,7 +144,7 @@ __device__ __forceinline__ unsigned long long lb_wait(const unsigned long long* 
             return lb_pack(seq, kLbPrefix, 0);
         }
         __nanosleep(32);
-        word = ld_acquire_u64(w);
+        word = ld_relaxed_u64(w);
     }
     return word;
 }
@@ -150,7 +153,7 @@ __device__ __forceinline__ unsigned long long lb_wait(const unsigned long long* 
 // (waiting, bounded); on timeout 0 and `timed_out` set.
 __device__ __forceinline__ int32_t bank_wait(const unsigned long long* w, unsigned tiles, long long deadline,
                                              bool& timed_out) {
-    unsigned long long word = ld_acquire_u64(w);
+    unsigned long long word = ld_relaxed_u64(w);
     uint32_t polls = 0;
     while (static_cast<unsigned>(word >> 32) != tiles) {
         if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
@@ -158,7 +161,7 @@ __device__ __forceinline__ int32_t bank_wait(const unsigned long long* w, unsign
             return 0;
         }
         __nanosleep(32);
-        word = ld_acquire_u64(w);
+        word = ld_relaxed_u64(w);
     }
     return static_cast<int32_t>(word & 0xffffffffull);
 }
@@ -369,7 +372,7 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     unsigned long long* mine = p.words + static_cast<int64_t>(b) * V;
     if (tid < V && !withhold) {
         const uint32_t c = static_cast<uint32_t>(sh.cnt[tid]);
-        st_release_u64(mine + tid, lb_pack(seq, j == 0 ? kLbPrefix : kLbAggregate, c));
+        st_relaxed_u64(mine + tid, lb_pack(seq, j == 0 ? kLbPrefix : kLbAggregate, c));
         atomicAdd(bank + s * V + tid, (1ull << 32) | c);
     }
 
@@ -452,7 +455,7 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
         sh.wex[tid] = wex;
         if (!withhold) {
             const uint32_t incl = static_cast<uint32_t>(wex + sh.cnt[tid]);
-            if (j > 0) st_release_u64(mine + tid, lb_pack(seq, kLbPrefix, incl));
+            if (j > 0) st_relaxed_u64(mine + tid, lb_pack(seq, kLbPrefix, incl));
         }
     }
     {
