@@ -419,6 +419,17 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
         sh.last_of_source = atomicAdd(p.src_arrive + s, 1u) == static_cast<unsigned>(p.tps - 1);
         sh.last_of_all = atomicAdd(p.arrive_all, 1u) == static_cast<unsigned>(p.n_tiles - 1);
     }
+    // the totals of the earlier sources (word i = s2 * V + v of the bank):
+    // first loads issued now, checked after the lookback, so the two round
+    // trips overlap
+    constexpr int kTotalsAhead = 4;
+    const int n_totals = s * V;
+    unsigned long long tw[kTotalsAhead];
+#pragma unroll
+    for (int k = 0; k < kTotalsAhead; ++k) {
+        const int i = tid + k * B;
+        tw[k] = i < n_totals ? ld_relaxed_u64(bank + i) : 0ull;
+    }
     int32_t wex = 0;  // thread v < V: exclusive prefix of value v within the source
     if (j > 0) {
         const int seg_lo = s * p.tps;  // first tile of the source
@@ -459,14 +470,19 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
         }
     }
     {
-        int s2 = tid / V, v = tid - (tid / V) * V;
-        for (int i = tid; i < s * V; i += B, s2 += B / V, v += B % V) {
-            if (v >= V) {
-                v -= V;
-                ++s2;
+        const unsigned tps = static_cast<unsigned>(p.tps);
+#pragma unroll
+        for (int k = 0; k < kTotalsAhead; ++k) {
+            const int i = tid + k * B;
+            if (i < n_totals) {
+                const int32_t t = static_cast<unsigned>(tw[k] >> 32) == tps
+                                      ? static_cast<int32_t>(tw[k] & 0xffffffffull)
+                                      : bank_wait(bank + i, tps, deadline, timed_out);
+                atomicAdd(&sh.xs[i % V], t);
             }
-            atomicAdd(&sh.xs[v], bank_wait(bank + s2 * V + v, static_cast<unsigned>(p.tps), deadline, timed_out));
         }
+        for (int i = tid + kTotalsAhead * B; i < n_totals; i += B)
+            atomicAdd(&sh.xs[i % V], bank_wait(bank + i, tps, deadline, timed_out));
     }
     __syncthreads();
 
