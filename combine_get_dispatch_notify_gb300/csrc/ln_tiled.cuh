@@ -486,6 +486,20 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     }
     __syncthreads();
 
+    // The last tile of the source / of the call loads the expert counts now
+    // (with no more experts than threads), so the round trip overlaps the
+    // stores of step D; they are written out in E2
+    const unsigned copy_out = (sh.last_of_source ? 1u : 0u) | (sh.last_of_all ? 2u : 0u);
+    const bool copy_early = E <= B;
+    int32_t ex_src = 0, ex_all = 0;
+    if (copy_out && copy_early) {
+        __threadfence();
+        if (tid < E) {
+            if (copy_out & 1u) ex_src = __ldcg(p.acc + static_cast<int64_t>(s) * kAccExperts + tid);
+            if (copy_out & 2u) ex_all = __ldcg(p.acc_all + tid);
+        }
+    }
+
     // D1. send_pos[s][t][r]: row of (s,t) inside r's region, or -1.  A
     //     thread keeps 4 ranks (their row offsets in registers) and steps
     //     through tokens; 16-byte loads of ballots and prefixes, 16-byte stores
@@ -592,24 +606,38 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     }
     if (timed_out) flag_error(p.a.status, EP_DEV_TIMEOUT);
 
-    // E2. the last tile of the source / of the call reads the expert counts
-    //     out, every tile having added its own before arriving
-    if (sh.last_of_source) {
-        __threadfence();
-        for (int e = tid; e < E; e += B) {
-            int32_t* a = p.acc + static_cast<int64_t>(s) * kAccExperts + e;
-            p.num_tokens_per_expert[static_cast<int64_t>(s) * E + e] = __ldcg(a);
-            *a = 0;
+    // E2. the last tile of the source / of the call writes the expert counts
+    //     out (every tile added its own before arriving) and clears them
+    if (copy_out & 1u) {
+        if (copy_early) {
+            if (tid < E) {
+                p.num_tokens_per_expert[static_cast<int64_t>(s) * E + tid] = ex_src;
+                p.acc[static_cast<int64_t>(s) * kAccExperts + tid] = 0;
+            }
+        } else {
+            __threadfence();
+            for (int e = tid; e < E; e += B) {
+                int32_t* a = p.acc + static_cast<int64_t>(s) * kAccExperts + e;
+                p.num_tokens_per_expert[static_cast<int64_t>(s) * E + e] = __ldcg(a);
+                *a = 0;
+            }
         }
         if (tid == 0) atomicExch(p.src_arrive + s, 0u);
     }
-    if (sh.last_of_all) {
-        __threadfence();
-        for (int e = tid; e < E; e += B) {
-            long long sum = __ldcg(p.acc_all + e);
-            p.acc_all[e] = 0;
-            sum = (sum + p.align - 1) / p.align * p.align;
-            p.a.num_recv_tokens_per_expert[e] = static_cast<int32_t>(sum);
+    if (copy_out & 2u) {
+        auto rounded = [&](long long c) { return static_cast<int32_t>((c + p.align - 1) / p.align * p.align); };
+        if (copy_early) {
+            if (tid < E) {
+                p.acc_all[tid] = 0;
+                p.a.num_recv_tokens_per_expert[tid] = rounded(ex_all);
+            }
+        } else {
+            __threadfence();
+            for (int e = tid; e < E; e += B) {
+                const long long sum = __ldcg(p.acc_all + e);
+                p.acc_all[e] = 0;
+                p.a.num_recv_tokens_per_expert[e] = rounded(sum);
+            }
         }
         if (tid == 0) atomicExch(p.arrive_all, 0u);
     }
