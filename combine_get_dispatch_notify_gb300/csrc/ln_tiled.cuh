@@ -16,7 +16,7 @@
 //      a tile publishes its counts, and adds them into its source's total
 //      words (one 64-bit atomic per value: the tiles that have added in the
 //      high half, the running total in the low half); adds its histogram into
-//      the source's and the call's expert counters (red.add); then looks back
+//      the source's and the call's expert counter words the same way; looks back
 //      over the earlier tiles of its own source (decoupled lookback, 32
 //      predecessors per probe, every value at once) and adds the totals of
 //      the earlier source ranks, each read once all of that source's tiles
@@ -29,11 +29,10 @@
 //      gbl/rdma_channel_prefix_matrix at its end); for the source's last
 //      tile the source's counts and rank prefix;
 //   E. the last tile - it holds the global prefix at the very end - writes
-//      the receive counts, recv_base and the node-level
-//      receive prefix; every tile arrives on two counters, and the last tile
-//      of a source copies the source's expert counts out (clearing them for
-//      the next call), the last tile of the call does the same for the
-//      per-expert receive counts.
+//      the receive counts, recv_base and the node-level receive prefix; the
+//      thread whose add completed an expert counter word (the source's last
+//      tile to add, or the call's) writes that count out and clears the word
+//      for the next call.
 // Only steps C and E wait, and only on tiles with smaller numbers (earlier
 // tiles of the source; the tiles of earlier sources), which publish what is
 // waited for before they wait on anything.  A smaller number is either the
@@ -58,11 +57,11 @@ constexpr int kAccExperts = 8192;
 constexpr int kBankWords = 32 * 36;  // source total words of one call: [R][V], R <= 32, V <= 36
 
 // Workspace of the tiled form, all offsets in bytes from its start:
-//   header     ticket word, arrival counters (all tiles, finished tiles, one
-//              per source) and the `ready` word;
-//   acc        expert counts of the running call, per source [32][8192] and
-//              summed over sources [8192], int32, whatever the shape (so a
-//              later call of another shape finds them zero);
+//   header     ticket word, the finished-tiles counter and the `ready` word;
+//   acc        expert counter words of the running call (64-bit: tiles that
+//              have added in [63:32], count in [31:0]), per source
+//              [32][8192] and summed over sources [8192], whatever the shape
+//              (so a later call of another shape finds them zero);
 //   banks      two banks of source total words [32 * 36] (64-bit: tiles in
 //              [63:32], total in [31:0]); a call adds into the bank of its
 //              sequence number's parity, and its first tile clears the other
@@ -70,23 +69,21 @@ constexpr int kBankWords = 32 * 36;  // source total words of one call: [R][V], 
 //   words      within-source lookback words [n_tiles][V], tagged with the
 //              writing call's sequence number, so what an earlier call of any
 //              shape left there never reads as this call's.
-// The header counters, acc and banks must be zero before the first call;
-// every call leaves the counters and acc zero, and the next call's bank.
+// The header, acc and banks must be zero before the first call; every call
+// leaves the header counters and acc zero, and the next call's bank.
 struct TiledWorkspace {
-    size_t ticket, arrive_all, finished, ready, src_arrive, acc, acc_all, banks, words, total;
+    size_t ticket, finished, ready, acc, acc_all, banks, words, total;
 };
 
 inline TiledWorkspace tiled_workspace_layout(int R, int N, long long n_tiles) {
     TiledWorkspace w;
     const size_t V = static_cast<size_t>(R + N);
     w.ticket = 0;
-    w.arrive_all = 8;
     w.finished = 12;
     w.ready = 16;
-    w.src_arrive = 64;  // R <= 32 counters
     w.acc = 256;
-    w.acc_all = w.acc + sizeof(int32_t) * static_cast<size_t>(kAccRanks) * kAccExperts;
-    w.banks = w.acc_all + sizeof(int32_t) * static_cast<size_t>(kAccExperts);
+    w.acc_all = w.acc + sizeof(unsigned long long) * static_cast<size_t>(kAccRanks) * kAccExperts;
+    w.banks = w.acc_all + sizeof(unsigned long long) * static_cast<size_t>(kAccExperts);
     w.words = w.banks + sizeof(unsigned long long) * 2 * static_cast<size_t>(kBankWords);
     w.total = w.words + sizeof(unsigned long long) * static_cast<size_t>(n_tiles) * V;
     return w;
@@ -100,12 +97,10 @@ struct TiledLnArgs {
     uint8_t* is_token_in_rank;
     NotifyArgs a;  // outputs of the notify step (its count-input fields are unused)
     unsigned long long* ticket;  // [63:32] sequence number of the last call, [31:0] tickets taken
-    unsigned* arrive_all;        // tiles whose expert counts are in, this call
     unsigned* finished;          // tiles whose outputs are written, this call (signal_ready)
     unsigned long long* ready;   // sequence number of the last call whose row map is complete
-    unsigned* src_arrive;        // [R] tiles of each source whose expert counts are in
-    int32_t* acc;                // [32][8192] per-source expert counts of the running call
-    int32_t* acc_all;            // [8192] expert counts summed over sources
+    unsigned long long* acc;      // [32][8192] per-source expert counter words of the running call
+    unsigned long long* acc_all;  // [8192] expert counter words summed over sources
     unsigned long long* banks;   // [2][32 * 36] source total words, by call parity
     unsigned long long* words;   // [n_tiles][V] lookback words, within each source
     int R, T, K, E, N, E_loc, C, q, align, V, TT, tps, n_tiles;
@@ -184,7 +179,6 @@ struct TiledShared {
     uint32_t lb[kLbSlots][kTiledMaxValues];  // low halves of the words of one lookback probe
     int ticket;
     unsigned seq;
-    int last_of_source, last_of_all;
 };
 
 // Tickets: a CTA's first tile is its block index; every CTA takes one ticket
@@ -250,6 +244,22 @@ __device__ __forceinline__ void tiled_prefetch_ids(const TiledLnArgs& p, int b) 
     if (t1 > t0)
         prefetch_l2(p.topk_idx + (static_cast<int64_t>(s) * p.T + t0) * p.K,
                     static_cast<size_t>(t1 - t0) * p.K * sizeof(int64_t));
+}
+
+// Expert e of source s after this tile's adds (h: the tile's count; o_src /
+// o_all: the counter words before them).  The add that completed a word
+// writes its count out and clears it.
+__device__ __forceinline__ void tiled_expert_done(const TiledLnArgs& p, int s, int e, int32_t h,
+                                                  unsigned long long o_src, unsigned long long o_all) {
+    if (static_cast<unsigned>(o_src >> 32) == static_cast<unsigned>(p.tps - 1)) {
+        p.num_tokens_per_expert[static_cast<int64_t>(s) * p.E + e] = static_cast<int32_t>(o_src) + h;
+        p.acc[static_cast<int64_t>(s) * kAccExperts + e] = 0ull;
+    }
+    if (static_cast<unsigned>(o_all >> 32) == static_cast<unsigned>(p.n_tiles - 1)) {
+        const long long c = static_cast<long long>(static_cast<int32_t>(o_all)) + h;
+        p.a.num_recv_tokens_per_expert[e] = static_cast<int32_t>((c + p.align - 1) / p.align * p.align);
+        p.acc_all[e] = 0ull;
+    }
 }
 
 // One tile b (of source b / tps); returns the CTA's next tile, or -1.  Thread
@@ -400,25 +410,20 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     // C. two-level scan: (1, above) the counts are published and added into
     //    the source's totals; (2) look back over the source's earlier tiles;
     //    (3) sum the totals of the earlier sources.
-    // The tile's expert counts into the source's and the call's (red.add),
-    // then, while the other warps look back, one thread of the last warp
-    // arrives on their counters (after the barrier its fence orders every
-    // thread's adds before the arrival), so the last tile of the source / of
-    // the call knows to read them out at its end
-    for (int e = tid; e < E; e += B) {
-        const int32_t h = hist[e];
-        if (h) {
-            atomicAdd(p.acc + static_cast<int64_t>(s) * kAccExperts + e, h);
-            atomicAdd(p.acc_all + e, h);
-        }
+    // The tile's expert counts into the source's and the call's counter
+    // words, every expert whether its count is zero or not; with no more
+    // experts than threads the adds go out here and their results (which
+    // say whether this add completed the word) are read in E2
+    const bool experts_early = E <= B;
+    unsigned long long ex_src = 0, ex_all = 0;
+    int32_t ex_h = 0;
+    if (experts_early && tid < E) {
+        ex_h = hist[tid];
+        const unsigned long long add = (1ull << 32) | static_cast<uint32_t>(ex_h);
+        ex_src = atomicAdd(p.acc + static_cast<int64_t>(s) * kAccExperts + tid, add);
+        ex_all = atomicAdd(p.acc_all + tid, add);
     }
-    __syncthreads();
     const int Bl = B - kWarp;  // threads of the lookback loads
-    if (tid == Bl) {
-        __threadfence();
-        sh.last_of_source = atomicAdd(p.src_arrive + s, 1u) == static_cast<unsigned>(p.tps - 1);
-        sh.last_of_all = atomicAdd(p.arrive_all, 1u) == static_cast<unsigned>(p.n_tiles - 1);
-    }
     // the totals of the earlier sources (word i = s2 * V + v of the bank):
     // first loads issued now, checked after the lookback, so the two round
     // trips overlap
@@ -485,20 +490,6 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
             atomicAdd(&sh.xs[i % V], bank_wait(bank + i, tps, deadline, timed_out));
     }
     __syncthreads();
-
-    // The last tile of the source / of the call loads the expert counts now
-    // (with no more experts than threads), so the round trip overlaps the
-    // stores of step D; they are written out in E2
-    const unsigned copy_out = (sh.last_of_source ? 1u : 0u) | (sh.last_of_all ? 2u : 0u);
-    const bool copy_early = E <= B;
-    int32_t ex_src = 0, ex_all = 0;
-    if (copy_out && copy_early) {
-        __threadfence();
-        if (tid < E) {
-            if (copy_out & 1u) ex_src = __ldcg(p.acc + static_cast<int64_t>(s) * kAccExperts + tid);
-            if (copy_out & 2u) ex_all = __ldcg(p.acc_all + tid);
-        }
-    }
 
     // D1. send_pos[s][t][r]: row of (s,t) inside r's region, or -1.  A
     //     thread keeps 4 ranks (their row offsets in registers) and steps
@@ -606,40 +597,28 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     }
     if (timed_out) flag_error(p.a.status, EP_DEV_TIMEOUT);
 
-    // E2. the last tile of the source / of the call writes the expert counts
-    //     out (every tile added its own before arriving) and clears them
-    if (copy_out & 1u) {
-        if (copy_early) {
-            if (tid < E) {
-                p.num_tokens_per_expert[static_cast<int64_t>(s) * E + tid] = ex_src;
-                p.acc[static_cast<int64_t>(s) * kAccExperts + tid] = 0;
+    // E2. an add that completed an expert counter word - the source's
+    //     tps-th, the call's n_tiles-th - makes its thread write the count out
+    //     and clear the word for the next call
+    if (experts_early) {
+        if (tid < E) tiled_expert_done(p, s, tid, ex_h, ex_src, ex_all);
+    } else {
+        constexpr int kBatch = 4;
+        for (int e0 = tid; e0 < E; e0 += kBatch * B) {
+            unsigned long long o_src[kBatch], o_all[kBatch];
+            int32_t h[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int e = e0 + u * B;
+                h[u] = e < E ? hist[e] : 0;
+                const unsigned long long add = (1ull << 32) | static_cast<uint32_t>(h[u]);
+                o_src[u] = e < E ? atomicAdd(p.acc + static_cast<int64_t>(s) * kAccExperts + e, add) : 0ull;
+                o_all[u] = e < E ? atomicAdd(p.acc_all + e, add) : 0ull;
             }
-        } else {
-            __threadfence();
-            for (int e = tid; e < E; e += B) {
-                int32_t* a = p.acc + static_cast<int64_t>(s) * kAccExperts + e;
-                p.num_tokens_per_expert[static_cast<int64_t>(s) * E + e] = __ldcg(a);
-                *a = 0;
-            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (e0 + u * B < E) tiled_expert_done(p, s, e0 + u * B, h[u], o_src[u], o_all[u]);
         }
-        if (tid == 0) atomicExch(p.src_arrive + s, 0u);
-    }
-    if (copy_out & 2u) {
-        auto rounded = [&](long long c) { return static_cast<int32_t>((c + p.align - 1) / p.align * p.align); };
-        if (copy_early) {
-            if (tid < E) {
-                p.acc_all[tid] = 0;
-                p.a.num_recv_tokens_per_expert[tid] = rounded(ex_all);
-            }
-        } else {
-            __threadfence();
-            for (int e = tid; e < E; e += B) {
-                const long long sum = __ldcg(p.acc_all + e);
-                p.acc_all[e] = 0;
-                p.a.num_recv_tokens_per_expert[e] = rounded(sum);
-            }
-        }
-        if (tid == 0) atomicExch(p.arrive_all, 0u);
     }
     if (p.signal_ready) {
         // the row map (send_pos, recv_base) is complete once every tile is here
@@ -691,12 +670,10 @@ inline TiledLnArgs tiled_args(const Shape& sh, int TT, const int64_t* topk_idx, 
     const TiledWorkspace w = tiled_workspace_layout(sh.R, sh.N, p.n_tiles);
     char* base = static_cast<char*>(workspace);
     p.ticket = reinterpret_cast<unsigned long long*>(base + w.ticket);
-    p.arrive_all = reinterpret_cast<unsigned*>(base + w.arrive_all);
     p.finished = reinterpret_cast<unsigned*>(base + w.finished);
     p.ready = reinterpret_cast<unsigned long long*>(base + w.ready);
-    p.src_arrive = reinterpret_cast<unsigned*>(base + w.src_arrive);
-    p.acc = reinterpret_cast<int32_t*>(base + w.acc);
-    p.acc_all = reinterpret_cast<int32_t*>(base + w.acc_all);
+    p.acc = reinterpret_cast<unsigned long long*>(base + w.acc);
+    p.acc_all = reinterpret_cast<unsigned long long*>(base + w.acc_all);
     p.banks = reinterpret_cast<unsigned long long*>(base + w.banks);
     p.words = reinterpret_cast<unsigned long long*>(base + w.words);
     return p;

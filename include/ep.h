@@ -249,9 +249,10 @@ ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
                              int32_t* status, int32_t* host_num_recv_tokens, cudaStream_t stream);
 
 /* Bytes of workspace ep_layout_notify (and ep_layout_notify_dispatch) needs
- * for `shape`, or 0 for an invalid shape: a 256-byte header, 1 MiB + 32 KiB
- * of per-expert counters, 18 KiB of per-source totals (two banks of 32 * 36
- * 64-bit words) and 8 * (R + N) bytes per tile. */
+ * for `shape`, or 0 for an invalid shape: a 256-byte header, 2 MiB + 64 KiB
+ * of per-expert counter words (64-bit, [32][8192] + [8192]), 18 KiB of
+ * per-source totals (two banks of 32 * 36 64-bit words) and 8 * (R + N) bytes
+ * per tile. */
 size_t ep_layout_notify_workspace_bytes(const ep_shape_t* shape);
 
 /* Which kernel ep_layout_notify runs for this shape on the current device:

@@ -190,7 +190,7 @@ def test_layout_notify_workspace_bytes_follow_the_documented_formula(ep):
         while tt < 8192 and R * -(-T // tt) > 16384:
             tt *= 2
         tiles = R * (-(-T // tt) if T > 0 else 1)
-        return 256 + (1 << 20) + (32 << 10) + (18 << 10) + 8 * V * tiles
+        return 256 + (2 << 20) + (64 << 10) + (18 << 10) + 8 * V * tiles
 
     for R, T in [(1, 0), (2, 1), (3, 41), (8, 4096), (16, 8192), (32, 16384), (32, 20000), (16, 300),
                  (32, 2 ** 25 - 1)]:  # R*T just under 2^30

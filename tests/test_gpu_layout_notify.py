@@ -238,7 +238,7 @@ def _tiled_ws_bytes(w: Workload, tile_tokens: int) -> int:
     if tile_tokens == 0:
         return ep.ep_layout_notify_workspace_bytes(sh)
     tiles = w.R * (max(1, -(-w.T // tile_tokens)) if w.T > 0 else 1)
-    return 256 + (1 << 20) + (32 << 10) + (18 << 10) + 8 * (w.R + w.N) * tiles
+    return 256 + (2 << 20) + (64 << 10) + (18 << 10) + 8 * (w.R + w.N) * tiles
 
 
 TILED_SIZES = (32, 96, 512, 0)
@@ -279,11 +279,10 @@ def test_tiled_workspace_serves_shapes_in_turn_and_stays_clean():
         assert ep.ep_sync_status(status) == ep.EP_OK
         check_layout_notify(lay, nt, lay_ref, nt_ref)
         head = ws[:256].cpu()
-        assert (head[8:16] == 0).all()                               # tiles arrived / finished
-        assert (head[64:192] == 0).all()                             # tiles arrived per source
-        assert int((ws[256:256 + (1 << 20) + (32 << 10)] != 0).sum()) == 0  # expert counters
+        assert (head[8:16] == 0).all()                               # finished-tiles counter
+        assert int((ws[256:256 + (2 << 20) + (64 << 10)] != 0).sum()) == 0  # expert counters
         seq = int(head[:8].numpy().view(np.uint64)[0]) >> 32                # this call's sequence number
-        banks = 256 + (1 << 20) + (32 << 10)
+        banks = 256 + (2 << 20) + (64 << 10)
         nxt = banks + ((seq + 1) & 1) * (9 << 10)
         assert int((ws[nxt:nxt + (9 << 10)] != 0).sum()) == 0               # the next call's source totals
 
@@ -362,7 +361,7 @@ def test_tiled_bad_expert_id_reports_status():
     clean[20, 299, 5] = -1
     lay_ref, nt_ref = _oracle(w, clean)
     check_layout_notify(lay, nt, lay_ref, nt_ref)
-    assert int((ws[256:256 + (1 << 20) + (32 << 10)] != 0).sum()) == 0
+    assert int((ws[256:256 + (2 << 20) + (64 << 10)] != 0).sum()) == 0
 
 
 def test_tiled_every_expert_counter_in_use():
@@ -374,4 +373,4 @@ def test_tiled_every_expert_counter_in_use():
     sh, lay, nt, status, ws = _tiled(w, idx, 32)
     assert ep.ep_sync_status(status) == ep.EP_OK
     check_layout_notify(lay, nt, lay_ref, nt_ref)
-    assert int((ws[256:256 + (1 << 20) + (32 << 10)] != 0).sum()) == 0
+    assert int((ws[256:256 + (2 << 20) + (64 << 10)] != 0).sum()) == 0
