@@ -89,6 +89,24 @@ def host_headroom():
     torch.cuda._sleep(HEADROOM_CYCLES)
 
 
+def launch_floor_us(stream, flush, n: int) -> float:
+    """CUDA events around a kernel that does nothing (torch's spin kernel for
+    zero cycles), after the same L2 flush and host headroom as the per-call
+    timings: the floor that every single-launch figure below carries."""
+    ts = []
+    for i in range(n + 3):
+        flush.fill_(1)
+        host_headroom()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        torch.cuda._sleep(0)
+        b.record(stream)
+        if i >= 3:
+            ts.append((a, b))
+    torch.cuda.synchronize()
+    return round(statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3, 2)
+
+
 def step_bytes_of(nb: dict) -> int:
     """Algorithmic bytes of one whole step: layout + notify as one call, dispatch, combine."""
     return nb["layout_notify"] + nb["dispatch"] + nb["combine"]
@@ -475,6 +493,7 @@ def per_config_leg(name: str, args, dev, peak: float) -> dict:
                 ev_ops.append(e)
             torch.cuda.synchronize(dev)
             t1 = time.time()
+            floor = launch_floor_us(stream, flush, args.steps)
         assert ep.ep_sync_status(pipe.status, stream) == ep.EP_OK, f"{name}: device status not OK after timing"
     step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_step)
     per_op = {}
@@ -492,7 +511,7 @@ def per_config_leg(name: str, args, dev, peak: float) -> dict:
            "value": round(sb / (step_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "tokens_per_s": round(w.R * w.T / (step_ms * 1e-3), 1), "rows_dispatched": P,
            "layout_notify_form": "cluster" if step.ln_form == 1 else "tiled",
-           "per_op": per_op, "clocks": sampler.summary(t0 - 0.45, t1 + 0.05)}
+           "per_op": per_op, "launch_floor_us": floor, "clocks": sampler.summary(t0 - 0.45, t1 + 0.05)}
     del step, g, pipe, x_d, idx_d, wt_d, flush
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
@@ -666,6 +685,9 @@ def run_ours(args, w):
                  "note": "ep_layout_notify_dispatch (one launch) + ep_combine, CUDA graph, L2 flushed; "
                          "the headline step is the chain ep_layout_notify -> ep_dispatch -> ep_combine"}
         del gf
+
+    with torch.cuda.stream(stream):
+        floor_us = launch_floor_us(stream, flush, args.steps)
 
     # FP8 rows (the pages' 1-byte element size with per-token scales): dispatch alone
     fp8 = None
@@ -928,6 +950,9 @@ def run_ours(args, w):
             "tokens_per_s": round(tokens * world / (ms * 1e-3), 1),
             "rows_dispatched": P,
             "per_op": per_op,
+            "launch_floor_us": floor_us,
+            "launch_floor_note": "CUDA events around an empty kernel after the same L2 flush and host headroom: "
+                                 "every per_op / fp8_dispatch figure (one launch between two events) includes it",
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
