@@ -270,11 +270,12 @@ ep_status_t layout_notify_args(const Shape& sh, const int64_t* topk_idx, int32_t
 }
 
 // Which kernel ep_layout_notify runs: 1 = one thread-block cluster of R CTAs
-// (R <= 16, T <= 2048, R * T <= 16384 and the cluster fits: there it beats
-// the tiled form, e.g. 13.4 vs 16.4 us at R = 16, T = 1024; with more tokens
-// per CTA it falls behind), 2 = the tiled form (any shape).
-constexpr long long kClusterMaxTokensPerRank = 2048;
-constexpr long long kClusterMaxTokens = 16384;
+// (R <= 16, T <= 1024, R * T <= 8192 and the cluster fits: there it is as
+// fast as the tiled form or faster, e.g. 10.0 vs 10.3 us at R = 16, T = 128
+// and 11.7 vs 12.3 us at T = 512; with more tokens per CTA it falls behind,
+// 13.5 vs 12.3 us at T = 1024), 2 = the tiled form (any shape).
+constexpr long long kClusterMaxTokensPerRank = 1024;
+constexpr long long kClusterMaxTokens = 8192;
 
 int layout_notify_form(const Shape& sh) {
     if (sh.T <= kClusterMaxTokensPerRank && static_cast<long long>(sh.R) * sh.T <= kClusterMaxTokens &&

@@ -208,20 +208,23 @@ ep_status_t ep_notify_dispatch(const ep_shape_t* shape, const uint8_t* is_token_
  * 1-3).  Every output of both calls is written, with the same values.  Always
  * one kernel, in one of two forms (ep_layout_notify_fused tells which):
  *
- *   cluster form (R <= 16, T <= 2048, R*T <= 16384, and a thread-block
+ *   cluster form (R <= 16, T <= 1024, R*T <= 8192, and a thread-block
  *   cluster of R CTAs fits on the device): CTA s counts source rank s's tokens and keeps one
  *   ballot word per 32 tokens and destination in shared memory; the counts
  *   are exchanged through distributed shared memory and one cluster barrier,
  *   so no workspace traffic and no second pass over is_token_in_rank.
  *
- *   tiled form (every other shape): CTAs take tiles of up to 512 tokens of
- *   one source rank from a ticket in (source rank, tile) order ([CH]
- *   channels are tiles of the same kind); per-rank counts pass through a
- *   single-pass decoupled-lookback scan over all tiles ([AR] 3.2), whose
- *   exclusive prefix is directly each tile's first row in every
- *   destination's region; the per-source and per-rank results are computed
- *   by the last tile of each source and the last source to finish.  A tile
- *   waits only for tiles with smaller tickets, every wait is bounded.
+ *   tiled form (every other shape): CTAs work on tiles of tokens of one
+ *   source rank, numbered in (source rank, tile) order - a CTA's first tile
+ *   is its block index, later ones come from a ticket ([CH] channels are
+ *   tiles of the same kind); per-rank counts pass through a single-pass
+ *   scan ([AR] 3.2) - decoupled lookback within each source, per-source
+ *   totals in self-counting 64-bit words - whose exclusive prefix is
+ *   directly each tile's first row in every destination's region; the
+ *   per-source results come from each source's last tile, the per-expert
+ *   counts from the add that completes each counter word, the per-rank
+ *   results from the last tile.  A tile waits only for tiles with smaller
+ *   numbers, every wait is bounded.
  *
  * Arguments: topk_idx and the four layout outputs as for
  * ep_get_dispatch_layout; the notify outputs and host_num_recv_tokens as for

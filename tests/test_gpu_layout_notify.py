@@ -1,6 +1,6 @@
 """ep_layout_notify (layout and notify in one call) vs the CPU oracle, element
 by element, through the C ABI: the cluster form on the shapes it takes (R <= 16,
-T <= 2048, R*T <= 16384), the tiled form on the others, and the tiled form forced on every
+T <= 1024, R*T <= 8192), the tiled form on the others, and the tiled form forced on every
 case with several tile sizes (ep_debug_layout_notify_tiled); all bit-exact."""
 from __future__ import annotations
 
@@ -26,7 +26,7 @@ def _lib():
 
 
 def _fused_expected(w: Workload) -> int:
-    return 1 if (w.R <= 16 and w.T <= 2048 and w.R * w.T <= 16384) else 2
+    return 1 if (w.R <= 16 and w.T <= 1024 and w.R * w.T <= 8192) else 2
 
 
 def _run(w: Workload, idx: torch.Tensor, host=None):
