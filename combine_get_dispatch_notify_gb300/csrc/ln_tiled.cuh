@@ -127,14 +127,26 @@ __device__ __forceinline__ int32_t lb_val(unsigned long long w) {
     return static_cast<int32_t>(w & ((1ull << 30) - 1));
 }
 
+// A thread's waits in one tile share one deadline, set by the first of them
+// that keeps polling (0 until then: a tile whose words are all there reads
+// no timer).  True once it has passed.
+__device__ __forceinline__ bool wait_expired(long long& deadline, long long limit_ns) {
+    const long long now = globaltimer_ns();
+    if (deadline == 0) {
+        deadline = now + limit_ns;
+        return false;
+    }
+    return now > deadline;
+}
+
 // Reads a tagged word of call `seq`, waiting (bounded) until it is published.
 // On timeout returns a prefix word of value 0 and sets `timed_out`.
-__device__ __forceinline__ unsigned long long lb_wait(const unsigned long long* w, unsigned seq,
-                                                      long long deadline, bool& timed_out) {
+__device__ __forceinline__ unsigned long long lb_wait(const unsigned long long* w, unsigned seq, long long limit_ns,
+                                                      long long& deadline, bool& timed_out) {
     unsigned long long word = ld_relaxed_u64(w);
     uint32_t polls = 0;
     while (static_cast<unsigned>(word >> 32) != seq) {
-        if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
+        if ((++polls & 15u) == 0 && wait_expired(deadline, limit_ns)) {
             timed_out = true;
             return lb_pack(seq, kLbPrefix, 0);
         }
@@ -146,12 +158,12 @@ __device__ __forceinline__ unsigned long long lb_wait(const unsigned long long* 
 
 // Total of a source once all `tiles` of its tiles have added into its word
 // (waiting, bounded); on timeout 0 and `timed_out` set.
-__device__ __forceinline__ int32_t bank_wait(const unsigned long long* w, unsigned tiles, long long deadline,
-                                             bool& timed_out) {
+__device__ __forceinline__ int32_t bank_wait(const unsigned long long* w, unsigned tiles, long long limit_ns,
+                                             long long& deadline, bool& timed_out) {
     unsigned long long word = ld_relaxed_u64(w);
     uint32_t polls = 0;
     while (static_cast<unsigned>(word >> 32) != tiles) {
-        if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
+        if ((++polls & 15u) == 0 && wait_expired(deadline, limit_ns)) {
             timed_out = true;
             return 0;
         }
@@ -281,7 +293,8 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     uint32_t* tmask = reinterpret_cast<uint32_t*>(hist + p.Ep);
     uint32_t* bal = tmask + p.TT;
     int32_t* pre = reinterpret_cast<int32_t*>(bal + J * Vp);
-    const long long deadline = globaltimer_ns() + p.wait_limit_ns;
+    const long long limit = p.wait_limit_ns;
+    long long deadline = 0;  // set by the first wait that keeps polling
     bool timed_out = false;
     unsigned long long ticket = 0;
     if (tid == taker) ticket = atomicAdd(p.ticket, 1ull);
@@ -449,7 +462,7 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
                 if (sh.fin[v]) continue;
                 const int pj = b - 1 - r0 - slot;  // before the source's first tile: prefix 0
                 const unsigned long long word =
-                    pj >= seg_lo ? lb_wait(p.words + static_cast<int64_t>(pj) * V + v, seq, deadline, timed_out)
+                    pj >= seg_lo ? lb_wait(p.words + static_cast<int64_t>(pj) * V + v, seq, limit, deadline, timed_out)
                                  : lb_pack(seq, kLbPrefix, 0);
                 sh.lb[slot][v] = static_cast<uint32_t>(word);  // [31:30] flag, [29:0] value
             }
@@ -482,12 +495,12 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
             if (i < n_totals) {
                 const int32_t t = static_cast<unsigned>(tw[k] >> 32) == tps
                                       ? static_cast<int32_t>(tw[k] & 0xffffffffull)
-                                      : bank_wait(bank + i, tps, deadline, timed_out);
+                                      : bank_wait(bank + i, tps, limit, deadline, timed_out);
                 atomicAdd(&sh.xs[i % V], t);
             }
         }
         for (int i = tid + kTotalsAhead * B; i < n_totals; i += B)
-            atomicAdd(&sh.xs[i % V], bank_wait(bank + i, tps, deadline, timed_out));
+            atomicAdd(&sh.xs[i % V], bank_wait(bank + i, tps, limit, deadline, timed_out));
     }
     __syncthreads();
 
@@ -588,7 +601,7 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
             int32_t run = 0;
             for (int m = 0; m < N; ++m) {
                 const int peer = m * kNodeSize + r % kNodeSize;
-                run += bank_wait(bank + peer * V + R + r / kNodeSize, static_cast<unsigned>(p.tps), deadline,
+                run += bank_wait(bank + peer * V + R + r / kNodeSize, static_cast<unsigned>(p.tps), limit, deadline,
                                  timed_out);
                 p.a.recv_rdma_rank_prefix_sum[static_cast<int64_t>(r) * N + m] = run;
             }
