@@ -30,9 +30,10 @@
 //      tile the source's counts and rank prefix;
 //   E. the last tile - it holds the global prefix at the very end - writes
 //      the receive counts, recv_base and the node-level receive prefix; the
-//      thread whose add completed an expert counter word (the source's last
-//      tile to add, or the call's) writes that count out and clears the word
-//      for the next call.
+//      thread whose add completed a source's expert counter word writes that
+//      count out, clears the word for the next call and adds the count into
+//      the call's word for the expert, whose R-th add does the same for the
+//      per-expert receive count.
 // Only steps C and E wait, and only on tiles with smaller numbers (earlier
 // tiles of the source; the tiles of earlier sources), which publish what is
 // waited for before they wait on anything.  A smaller number is either the
@@ -258,17 +259,21 @@ __device__ __forceinline__ void tiled_prefetch_ids(const TiledLnArgs& p, int b) 
                     static_cast<size_t>(t1 - t0) * p.K * sizeof(int64_t));
 }
 
-// Expert e of source s after this tile's adds (h: the tile's count; o_src /
-// o_all: the counter words before them).  The add that completed a word
-// writes its count out and clears it.
+// Expert e of source s after this tile's add (h: the tile's count; o_src:
+// the source's counter word before it).  The add that completed the source's
+// word writes its count out, clears it and adds the source's count into the
+// call's word for e, whose R-th add writes the per-expert receive count
+// (rounded up to the alignment) out and clears that word.  One call-wide add
+// per source and expert, not per tile, keeps the call's words uncontended.
 __device__ __forceinline__ void tiled_expert_done(const TiledLnArgs& p, int s, int e, int32_t h,
-                                                  unsigned long long o_src, unsigned long long o_all) {
-    if (static_cast<unsigned>(o_src >> 32) == static_cast<unsigned>(p.tps - 1)) {
-        p.num_tokens_per_expert[static_cast<int64_t>(s) * p.E + e] = static_cast<int32_t>(o_src) + h;
-        p.acc[static_cast<int64_t>(s) * kAccExperts + e] = 0ull;
-    }
-    if (static_cast<unsigned>(o_all >> 32) == static_cast<unsigned>(p.n_tiles - 1)) {
-        const long long c = static_cast<long long>(static_cast<int32_t>(o_all)) + h;
+                                                  unsigned long long o_src) {
+    if (static_cast<unsigned>(o_src >> 32) != static_cast<unsigned>(p.tps - 1)) return;
+    const int32_t total = static_cast<int32_t>(o_src) + h;
+    p.num_tokens_per_expert[static_cast<int64_t>(s) * p.E + e] = total;
+    p.acc[static_cast<int64_t>(s) * kAccExperts + e] = 0ull;
+    const unsigned long long o_all = atomicAdd(p.acc_all + e, (1ull << 32) | static_cast<uint32_t>(total));
+    if (static_cast<unsigned>(o_all >> 32) == static_cast<unsigned>(p.R - 1)) {
+        const long long c = static_cast<long long>(static_cast<int32_t>(o_all)) + total;
         p.a.num_recv_tokens_per_expert[e] = static_cast<int32_t>((c + p.align - 1) / p.align * p.align);
         p.acc_all[e] = 0ull;
     }
@@ -428,13 +433,12 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     // experts than threads the adds go out here and their results (which
     // say whether this add completed the word) are read in E2
     const bool experts_early = E <= B;
-    unsigned long long ex_src = 0, ex_all = 0;
+    unsigned long long ex_src = 0;
     int32_t ex_h = 0;
     if (experts_early && tid < E) {
         ex_h = hist[tid];
-        const unsigned long long add = (1ull << 32) | static_cast<uint32_t>(ex_h);
-        ex_src = atomicAdd(p.acc + static_cast<int64_t>(s) * kAccExperts + tid, add);
-        ex_all = atomicAdd(p.acc_all + tid, add);
+        ex_src = atomicAdd(p.acc + static_cast<int64_t>(s) * kAccExperts + tid,
+                           (1ull << 32) | static_cast<uint32_t>(ex_h));
     }
     const int Bl = B - kWarp;  // threads of the lookback loads
     // the totals of the earlier sources (word i = s2 * V + v of the bank):
@@ -610,15 +614,15 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     }
     if (timed_out) flag_error(p.a.status, EP_DEV_TIMEOUT);
 
-    // E2. an add that completed an expert counter word - the source's
-    //     tps-th, the call's n_tiles-th - makes its thread write the count out
-    //     and clear the word for the next call
+    // E2. the add that completed a source's expert counter word (its
+    //     tps-th) makes its thread write the count out, clear the word and
+    //     pass the count on to the call's word (see tiled_expert_done)
     if (experts_early) {
-        if (tid < E) tiled_expert_done(p, s, tid, ex_h, ex_src, ex_all);
+        if (tid < E) tiled_expert_done(p, s, tid, ex_h, ex_src);
     } else {
         constexpr int kBatch = 4;
         for (int e0 = tid; e0 < E; e0 += kBatch * B) {
-            unsigned long long o_src[kBatch], o_all[kBatch];
+            unsigned long long o_src[kBatch];
             int32_t h[kBatch];
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
@@ -626,11 +630,10 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
                 h[u] = e < E ? hist[e] : 0;
                 const unsigned long long add = (1ull << 32) | static_cast<uint32_t>(h[u]);
                 o_src[u] = e < E ? atomicAdd(p.acc + static_cast<int64_t>(s) * kAccExperts + e, add) : 0ull;
-                o_all[u] = e < E ? atomicAdd(p.acc_all + e, add) : 0ull;
             }
 #pragma unroll
             for (int u = 0; u < kBatch; ++u)
-                if (e0 + u * B < E) tiled_expert_done(p, s, e0 + u * B, h[u], o_src[u], o_all[u]);
+                if (e0 + u * B < E) tiled_expert_done(p, s, e0 + u * B, h[u], o_src[u]);
         }
     }
     if (p.signal_ready) {
