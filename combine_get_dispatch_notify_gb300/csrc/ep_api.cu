@@ -370,7 +370,7 @@ int32_t ep_layout_notify_fused(const ep_shape_t* shape) {
 size_t ep_layout_notify_workspace_bytes(const ep_shape_t* shape) {
     ep::Shape sh;
     if (!ep::make_shape(shape, &sh)) return 0;
-    return ep::tiled_workspace_bytes(sh, ep::tiled_tile_tokens(sh, 0));
+    return ep::tiled_workspace_bytes(sh, ep::tiled_sizing_tokens(sh));
 }
 
 ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
@@ -392,8 +392,8 @@ ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
         recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens, num_rdma_recv_tokens,
         num_recv_tokens_per_expert, recv_base, send_pos, status, host_num_recv_tokens, &a);
     if (st != EP_OK) return st;
-    const int TT = ep::tiled_tile_tokens(sh, 0);
-    if (!ep::aligned16(workspace) || workspace_bytes < ep::tiled_workspace_bytes(sh, TT)) return EP_ERR_INVALID_ARG;
+    if (!ep::aligned16(workspace) || workspace_bytes < ep::tiled_workspace_bytes(sh, ep::tiled_sizing_tokens(sh)))
+        return EP_ERR_INVALID_ARG;
     if (ep::layout_notify_form(sh) == 1)
         return ep::from_cuda(ep::launch_layout_notify(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
                                                       num_tokens_per_expert, is_token_in_rank, a, stream));
@@ -423,10 +423,10 @@ ep_status_t ep_debug_layout_notify_tiled(
         recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens, num_rdma_recv_tokens,
         num_recv_tokens_per_expert, recv_base, send_pos, status, host_num_recv_tokens, &a);
     if (st != EP_OK) return st;
-    const int TT = ep::tiled_tile_tokens(sh, tile_tokens);
-    if (!ep::aligned16(workspace) || workspace_bytes < ep::tiled_workspace_bytes(sh, TT)) return EP_ERR_INVALID_ARG;
+    const int sized = tile_tokens > 0 ? tile_tokens : ep::tiled_sizing_tokens(sh);
+    if (!ep::aligned16(workspace) || workspace_bytes < ep::tiled_workspace_bytes(sh, sized)) return EP_ERR_INVALID_ARG;
     return ep::from_cuda(ep::launch_layout_notify_tiled(sh, topk_idx, num_tokens_per_rank, num_tokens_per_rdma_rank,
-                                                        num_tokens_per_expert, is_token_in_rank, a, workspace, TT,
+                                                        num_tokens_per_expert, is_token_in_rank, a, workspace, tile_tokens,
                                                         stall_tile, static_cast<long long>(wait_limit_us) * 1000LL,
                                                         stream));
 }
@@ -457,7 +457,7 @@ ep_status_t layout_notify_dispatch_common(
         recv_rdma_rank_prefix_sum, recv_channel_offset, num_recv_tokens, num_rdma_recv_tokens,
         num_recv_tokens_per_expert, recv_base, send_pos, status, host_num_recv_tokens, &a);
     if (st != EP_OK) return st;
-    if (!aligned16(workspace) || workspace_bytes < tiled_workspace_bytes(sh, tiled_tile_tokens(sh, 0)))
+    if (!aligned16(workspace) || workspace_bytes < tiled_workspace_bytes(sh, tiled_sizing_tokens(sh)))
         return EP_ERR_INVALID_ARG;
     if (capacity_rows < 0) return EP_ERR_INVALID_ARG;
     const long long tokens = static_cast<long long>(sh.R) * sh.T;

@@ -77,6 +77,7 @@ int max_blocks_per_sm(const void* kernel, int threads, size_t smem);
 // call leaves them zero).  stall_tile >= 0 (test hook): that tile never
 // publishes its lookback words.
 int tiled_tile_tokens(const Shape& sh, int requested);
+int tiled_sizing_tokens(const Shape& sh);
 size_t tiled_workspace_bytes(const Shape& sh, int TT);
 size_t tiled_workspace_zero_bytes();
 cudaError_t launch_layout_notify_tiled(const Shape& sh, const int64_t* topk_idx, int32_t* num_tokens_per_rank,

@@ -28,16 +28,26 @@ __global__ void __launch_bounds__(kTiledThreadsWide) layout_notify_tiled_kernel(
 
 }  // namespace
 
-// Tokens per tile: 512 (fewer when T is smaller), doubled (up to 8192) while
-// there are more than kMaxTiles tiles.  The workspace is sized for this tile
-// size; the launcher may take larger tiles (fewer of them).
-int tiled_tile_tokens(const Shape& sh, int requested) {
-    if (requested > 0) return requested;
-    int TT = 512;
+namespace {
+// `base` tokens per tile (fewer when T is smaller, a multiple of 32), doubled
+// (up to 8192) while there are more than kMaxTiles tiles.
+int tile_tokens_from(const Shape& sh, int base) {
+    int TT = base;
     if (sh.T < TT) TT = sh.T < kWarp ? kWarp : (sh.T + kWarp - 1) / kWarp * kWarp;
     while (TT < 8192 && static_cast<long long>(sh.R) * ((sh.T + TT - 1) / TT) > kMaxTiles) TT *= 2;
     return TT;
 }
+}  // namespace
+
+// Tokens per tile the launcher starts from: 512 by that rule.
+int tiled_tile_tokens(const Shape& sh, int requested) {
+    return requested > 0 ? requested : tile_tokens_from(sh, 512);
+}
+
+// Tokens per tile the workspace is sized for: 256 by that rule, so that it
+// holds at least as many tiles as the launcher takes (it never goes below
+// half of a tile of 512 or more tokens, and checks against this).
+int tiled_sizing_tokens(const Shape& sh) { return tile_tokens_from(sh, 256); }
 
 size_t tiled_workspace_bytes(const Shape& sh, int TT) {
     const long long tps = sh.T > 0 ? (sh.T + TT - 1) / TT : 1;
@@ -68,14 +78,16 @@ cudaError_t launch_layout_notify_tiled(const Shape& sh, const int64_t* topk_idx,
             TT *= 2;
         }
         // then the smallest tile (a multiple of 32) that still fits that wave:
-        // spreading the tokens over every resident slot shortens the busiest SM
-        if (TT > 512) {
+        // spreading the tokens over every resident slot shortens the busiest
+        // SM - within the tile count the workspace is sized for
+        if (TT >= 512) {
             const long long slots =
                 static_cast<long long>(max_blocks_per_sm(kernel, kTiledThreadsWide, tiled_smem_bytes(sh, TT))) * sms;
             const long long per_source = slots / sh.R;
+            const int ts = tiled_sizing_tokens(sh);
             if (per_source >= 1) {
                 const long long tt = ((sh.T + per_source - 1) / per_source + kWarp - 1) / kWarp * kWarp;
-                if (tt < TT && tt * 2 > TT) TT = static_cast<int>(tt);
+                if (tt < TT && tt * 2 > TT && tt >= ts) TT = static_cast<int>(tt);
             }
         }
     }

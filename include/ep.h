@@ -255,7 +255,8 @@ ep_status_t ep_layout_notify(const ep_shape_t* shape, const int64_t* topk_idx,
  * for `shape`, or 0 for an invalid shape: a 256-byte header, 2 MiB + 64 KiB
  * of per-expert counter words (64-bit, [32][8192] + [8192]), 18 KiB of
  * per-source totals (two banks of 32 * 36 64-bit words) and 8 * (R + N) bytes
- * per tile. */
+ * per tile, counting tiles of 256 tokens (T rounded up to 32 when smaller;
+ * doubled, up to 8192, while there would be more than 16384 tiles). */
 size_t ep_layout_notify_workspace_bytes(const ep_shape_t* shape);
 
 /* Which kernel ep_layout_notify runs for this shape on the current device:

@@ -186,7 +186,7 @@ def test_layout_notify_workspace_bytes_follow_the_documented_formula(ep):
     def want(R, T):
         N = 1 if R <= 8 else R // 8
         V = R + N
-        tt = 512 if T >= 512 else max(32, -(-T // 32) * 32)
+        tt = 256 if T >= 256 else max(32, -(-T // 32) * 32)
         while tt < 8192 and R * -(-T // tt) > 16384:
             tt *= 2
         tiles = R * (-(-T // tt) if T > 0 else 1)
