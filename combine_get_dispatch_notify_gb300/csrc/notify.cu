@@ -157,24 +157,35 @@ __device__ void per_rank_results(const NotifyKernelArgs& p, int32_t* s_nrecv,
 // Exclusive prefix of value v over blocks [seg_lo, b) (one warp).  Lanes read
 // 32 predecessors at once; the nearest published inclusive prefix ends the
 // walk, and the segment start acts as one with value 0.
+// A thread's waits share one deadline, set by the first of them that keeps
+// polling (0 until then: a block whose words are all there reads no timer).
+__device__ __forceinline__ bool notify_wait_expired(long long& deadline, long long limit_ns) {
+    const long long now = globaltimer_ns();
+    if (deadline == 0) {
+        deadline = now + limit_ns;
+        return false;
+    }
+    return now > deadline;
+}
+
 __device__ uint32_t segment_lookback(const NotifyKernelArgs& p, unsigned seq, int b, int seg_lo, int v,
-                                     int lane, long long deadline, bool& timed_out) {
+                                     int lane, long long& deadline, bool& timed_out) {
     uint32_t excl = 0;
     for (int j0 = b - 1; j0 >= seg_lo; j0 -= kWarp) {
         const int j = j0 - lane;
         unsigned long long word = pack_word(seq, kFlagPrefix, 0);
         if (j >= seg_lo) {
             const unsigned long long* w = p.words + static_cast<int64_t>(j) * p.V + v;
-            word = ld_acquire_u64(w);
+            word = ld_relaxed_u64(w);
             uint32_t polls = 0;
             while (word_seq(word) != seq) {  // not yet published by this call
-                if ((++polls & 15u) == 0 && globaltimer_ns() > deadline) {
+                if ((++polls & 15u) == 0 && notify_wait_expired(deadline, p.wait_limit_ns)) {
                     timed_out = true;
                     word = pack_word(seq, kFlagPrefix, 0);
                     break;
                 }
                 __nanosleep(32);
-                word = ld_acquire_u64(w);
+                word = ld_relaxed_u64(w);
             }
         }
         const unsigned pm = __ballot_sync(0xffffffffu, word_flag(word) == kFlagPrefix);
@@ -301,17 +312,17 @@ __global__ void __launch_bounds__(kNotifyThreads) notify_kernel(NotifyKernelArgs
         //    inclusive prefix directly), then look back within the source rank
         unsigned long long* mine = p.words + static_cast<int64_t>(b) * V;
         if (tid < V && b != p.stall_block)
-            st_release_u64(mine + tid, pack_word(seq, c == 0 ? kFlagPrefix : kFlagAggregate,
+            st_relaxed_u64(mine + tid, pack_word(seq, c == 0 ? kFlagPrefix : kFlagAggregate,
                                                  static_cast<uint32_t>(s_count[tid])));
         __syncthreads();
         bool timed_out = false;
-        const long long deadline = globaltimer_ns() + p.wait_limit_ns;
+        long long deadline = 0;  // set by the first wait that keeps polling
         for (int v = warp; v < V; v += kNotifyWarps) {
             const uint32_t ex = c == 0 ? 0u : segment_lookback(p, seq, b, s * C, v, lane, deadline, timed_out);
             if (lane == 0) {
                 s_segex[v] = static_cast<int32_t>(ex);
                 if (c != 0 && b != p.stall_block)
-                    st_release_u64(mine + v, pack_word(seq, kFlagPrefix, ex + static_cast<uint32_t>(s_count[v])));
+                    st_relaxed_u64(mine + v, pack_word(seq, kFlagPrefix, ex + static_cast<uint32_t>(s_count[v])));
             }
         }
         if (__any_sync(0xffffffffu, timed_out) && lane == 0) flag_error(p.a.status, EP_DEV_TIMEOUT);
