@@ -107,6 +107,31 @@ def launch_floor_us(stream, flush, n: int) -> float:
     return round(statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3, 2)
 
 
+def graph_prefix_ms(stream, flush, calls, steps: int, warmup: int) -> list:
+    """Mean CUDA-event time (ms) of one graph replay of calls[:1], calls[:2], ...
+    (L2 flushed before each replay): differences of neighbours are what each
+    call costs where the step runs it, the launch floor cancelling out."""
+    out = []
+    for n in range(1, len(calls) + 1):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls[:n]:
+                c()
+        ts = []
+        for i in range(warmup + steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            if i >= warmup:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        out.append(statistics.mean(a.elapsed_time(b) for a, b in ts))
+        del g
+    return out
+
+
 def step_bytes_of(nb: dict) -> int:
     """Algorithmic bytes of one whole step: layout + notify as one call, dispatch, combine."""
     return nb["layout_notify"] + nb["dispatch"] + nb["combine"]
@@ -688,6 +713,17 @@ def run_ours(args, w):
 
     with torch.cuda.stream(stream):
         floor_us = launch_floor_us(stream, flush, args.steps)
+        # each call's cost inside the step's graph: graph of the calls up to it
+        # minus the graph of the calls before it
+        pre = graph_prefix_ms(stream, flush, [step.layout_notify, step.dispatch, step.combine], args.steps,
+                              args.warmup)
+    in_step = {}
+    for k, ms_k in zip(("layout_notify", "dispatch", "combine"), (pre[0], pre[1] - pre[0], pre[2] - pre[1])):
+        ms_k = max(ms_k, 1e-6)
+        in_step[k] = {"us": round(ms_k * 1e3, 2),
+                      "frac_of_hbm": round(nbytes[k] / (ms_k * 1e-3) / 1e9 / measured_peak()[0], 4)}
+    in_step["note"] = ("graph replay of layout_notify, +dispatch, +combine (L2 flushed before each), each call "
+                       "the difference to the graph before it; layout_notify's figure includes the launch floor")
 
     # FP8 rows (the pages' 1-byte element size with per-token scales): dispatch alone
     fp8 = None
@@ -951,6 +987,7 @@ def run_ours(args, w):
             "rows_dispatched": P,
             "per_op": per_op,
             "launch_floor_us": floor_us,
+            "per_op_in_step": in_step,
             "launch_floor_note": "CUDA events around an empty kernel after the same L2 flush and host headroom: "
                                  "every per_op / fp8_dispatch figure (one launch between two events) includes it",
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
