@@ -8,15 +8,16 @@
 // from an atomic ticket counter:
 //   A. thread per (token, pair of top-k slots), up to 8 pairs of a thread
 //      loaded at once: expert histogram in shared memory and the token's rank
-//      mask; warp per 32 tokens writes the is_token_in_rank rows and one
-//      ballot word per destination rank / node;
-//   B. warp per value (rank or node): the tile's count and the exclusive
-//      prefix of every 32-token block inside the tile;
+//      mask; warp per 32 tokens writes the is_token_in_rank rows and gets
+//      one ballot word per destination rank / node (a 32x32 bit transpose of
+//      the tokens' masks), whose popcounts are the tile's counts;
+//   B. warp per value (rank or node): the exclusive prefix of every 32-token
+//      block inside the tile;
 //   C. two-level single-pass scan ([AR] 3.2: prefix sums by a block scan):
 //      a tile publishes its counts, and adds them into its source's total
 //      words (one 64-bit atomic per value: the tiles that have added in the
 //      high half, the running total in the low half); adds its histogram into
-//      the source's and the call's expert counter words the same way; looks back
+//      its source's expert counter words the same way; looks back
 //      over the earlier tiles of its own source (decoupled lookback, 32
 //      predecessors per probe, every value at once) and adds the totals of
 //      the earlier source ranks, each read once all of that source's tiles
