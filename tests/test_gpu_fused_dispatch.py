@@ -71,6 +71,8 @@ CASES = {
     "k32_repeats": Workload("e", R=16, T=97, H=64, E=512, K=32, C=7, routing="replace", mask=0.1),
     "one_token": Workload("e", R=16, T=1, H=64, E=16, K=3, C=1),
     "r24_many_tiles": Workload("e", R=24, T=1500, H=136, E=96, K=6, C=9, mask=0.1),
+    # 512 tiles of 512 tokens, more than the grid's CTAs: later tiles by ticket
+    "r32_more_tiles_than_ctas": Workload("e", R=32, T=8192, H=64, E=256, K=8, C=16, mask=0.05),
 }
 
 
