@@ -266,18 +266,31 @@ __device__ __forceinline__ void tiled_prefetch_ids(const TiledLnArgs& p, int b) 
 // call's word for e, whose R-th add writes the per-expert receive count
 // (rounded up to the alignment) out and clears that word.  One call-wide add
 // per source and expert, not per tile, keeps the call's words uncontended.
-__device__ __forceinline__ void tiled_expert_done(const TiledLnArgs& p, int s, int e, int32_t h,
-                                                  unsigned long long o_src) {
-    if (static_cast<unsigned>(o_src >> 32) != static_cast<unsigned>(p.tps - 1)) return;
-    const int32_t total = static_cast<int32_t>(o_src) + h;
+// The two halves: the source's word (returns whether this add completed it,
+// and the call's word before the source's count went in), then the call's.
+__device__ __forceinline__ bool tiled_expert_source(const TiledLnArgs& p, int s, int e, int32_t h,
+                                                    unsigned long long o_src, int32_t& total,
+                                                    unsigned long long& o_all) {
+    if (static_cast<unsigned>(o_src >> 32) != static_cast<unsigned>(p.tps - 1)) return false;
+    total = static_cast<int32_t>(o_src) + h;
     p.num_tokens_per_expert[static_cast<int64_t>(s) * p.E + e] = total;
     p.acc[static_cast<int64_t>(s) * kAccExperts + e] = 0ull;
-    const unsigned long long o_all = atomicAdd(p.acc_all + e, (1ull << 32) | static_cast<uint32_t>(total));
+    o_all = atomicAdd(p.acc_all + e, (1ull << 32) | static_cast<uint32_t>(total));
+    return true;
+}
+__device__ __forceinline__ void tiled_expert_call(const TiledLnArgs& p, int e, int32_t total,
+                                                  unsigned long long o_all) {
     if (static_cast<unsigned>(o_all >> 32) == static_cast<unsigned>(p.R - 1)) {
         const long long c = static_cast<long long>(static_cast<int32_t>(o_all)) + total;
         p.a.num_recv_tokens_per_expert[e] = static_cast<int32_t>((c + p.align - 1) / p.align * p.align);
         p.acc_all[e] = 0ull;
     }
+}
+__device__ __forceinline__ void tiled_expert_done(const TiledLnArgs& p, int s, int e, int32_t h,
+                                                  unsigned long long o_src) {
+    int32_t total = 0;
+    unsigned long long o_all = 0;
+    if (tiled_expert_source(p, s, e, h, o_src, total, o_all)) tiled_expert_call(p, e, total, o_all);
 }
 
 // One tile b (of source b / tps); returns the CTA's next tile, or -1.  Thread
@@ -509,6 +522,13 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     }
     __syncthreads();
 
+    // the source's half of the expert words now (the adds went out in C), so
+    // the call-wide add's round trip overlaps step D; its result is read in E2
+    bool ex_done = false;
+    int32_t ex_total = 0;
+    unsigned long long ex_all = 0;
+    if (experts_early && tid < E) ex_done = tiled_expert_source(p, s, tid, ex_h, ex_src, ex_total, ex_all);
+
     // D1. send_pos[s][t][r]: row of (s,t) inside r's region, or -1.  A
     //     thread keeps 4 ranks (their row offsets in registers) and steps
     //     through tokens; 16-byte loads of ballots and prefixes, 16-byte stores
@@ -616,10 +636,11 @@ __device__ inline int tiled_tile(const TiledLnArgs& p, TiledShared& sh, int32_t*
     if (timed_out) flag_error(p.a.status, EP_DEV_TIMEOUT);
 
     // E2. the add that completed a source's expert counter word (its
-    //     tps-th) makes its thread write the count out, clear the word and
-    //     pass the count on to the call's word (see tiled_expert_done)
+    //     tps-th) has made its thread write the count out, clear the word and
+    //     pass the count on to the call's word; the call's R-th add writes
+    //     the per-expert receive count (see tiled_expert_done)
     if (experts_early) {
-        if (tid < E) tiled_expert_done(p, s, tid, ex_h, ex_src);
+        if (ex_done) tiled_expert_call(p, tid, ex_total, ex_all);
     } else {
         constexpr int kBatch = 4;
         for (int e0 = tid; e0 < E; e0 += kBatch * B) {
