@@ -542,10 +542,10 @@ ep_status_t ep_debug_dispatch_stall(const ep_shape_t* shape, const uint16_t* x, 
  * Testing hook for the tiled form of ep_layout_notify.  Runs it whatever the
  * shape, with tiles of `tile_tokens` tokens (0: the default; else a multiple
  * of 32 in [32, 8192]; the workspace must then hold what that tile size
- * needs: 256 + 1 MiB + 32 KiB + 8 * (R + N) * R * ceil(T / tile)
- * + 8 * R * (R + N) bytes),
- * the tile with ticket `stall_tile` (-1: none) withholding its lookback
- * words, and every wait bounded by `wait_limit_us` microseconds (1 .. 2e6).
+ * needs: 256 + 2 MiB + 64 KiB + 18 KiB + 8 * (R + N) * R * ceil(T / tile)
+ * bytes), tile number `stall_tile` (-1: none) withholding its lookback words
+ * and its source-total adds, and every wait bounded by `wait_limit_us`
+ * microseconds (1 .. 2e6).
  * Tiles that wait on the withheld words give up, set EP_DEV_TIMEOUT and go
  * on, so the context stays usable; outputs are undefined after such a run.
  */
